@@ -1,0 +1,192 @@
+/*
+ * fa.h — C ABI of the GB300 (sm_103a) tiled online-softmax attention library
+ * (libfa_gb300.so).
+ *
+ * What it computes.  Exact scaled-dot-product attention
+ *     O = softmax(scale * Q K^T) V,   row-wise softmax,
+ * with Q n×d, K m×d, V m×dv and O n×dv per (batch, head)
+ * ("手搓 Attention：从三行循环到看懂 FlashAttention", §1).  The kernels never
+ * form the n×m score matrix in memory: they stream K/V tiles and keep, per
+ * query row, a running maximum m, a running sum l and an accumulator acc that
+ * are rescaled by alpha = exp(m_old - m_new) whenever the maximum grows
+ * (same page, §7 version 4; "S12 FlashAttention", 解法).  The log-sum-exp
+ * LSE = m + ln(l) (natural log, over the SCALED scores) is returned beside O.
+ *
+ * Conventions shared by every entry point.
+ *   - Pointers are DEVICE pointers owned by the caller, unless a parameter
+ *     says otherwise.  The library never allocates device memory for a call;
+ *     decode takes its split scratch from a caller-provided workspace.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and returns as soon as its launches are queued.
+ *   - Arguments are validated before anything is launched; on a bad argument
+ *     the call returns a non-zero fa_status and launches nothing.  The text of
+ *     the last failure on the calling thread is returned by fa_last_error().
+ *   - Problems that only the device can see (a block-table id out of range,
+ *     a pipeline wait that exceeded its time limit) set a device status word
+ *     instead of faulting; the affected outputs are left unspecified.
+ *     fa_get_device_status() synchronises the stream and reads and clears it.
+ *   - Layouts are dense row-major.  "BSHD" means [batch][token][head][dim].
+ *   - Grouped heads: query head h reads kv head h / (H / Hkv); H % Hkv == 0.
+ *   - bf16 values are IEEE bfloat16 bit patterns (uint16 storage); outputs O
+ *     are rounded to bf16 with round-to-nearest-even; LSE is float32.
+ *   - A query row that sees no key gets O = 0 and LSE = -inf.
+ *   - Causal: key j is visible to query i iff j <= i (0-based, top-left);
+ *     it requires n == m (per sequence for varlen).
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, H % Hkv != 0, misaligned pointer */
+    FA_ERR_UNSUPPORTED = 2,   /* valid but not implemented: d/dv/page_size outside the supported set,
+                                 causal with n != m, no sm_103a device */
+    FA_ERR_WORKSPACE = 3,     /* workspace pointer null or smaller than the size query returns */
+    FA_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed; fa_last_error() has the text */
+    FA_ERR_TIMEOUT = 5,       /* device status: a pipeline wait exceeded its limit */
+    FA_ERR_BAD_BLOCK_TABLE = 6 /* device status: a block-table id outside [0, num_pages) */
+} fa_status;
+
+/*
+ * fa_forward — bf16 attention forward, dense batch.
+ * Passage: "手搓 Attention" §1 (shapes and scale) and §7 version 4 (the
+ * recurrence); "S12 FlashAttention", 解法; whole causal tiles above the
+ * diagonal are skipped ("手搓 Attention" §6 and §7).
+ *
+ *   q    bf16 [B][n][H][d]       (BSHD)
+ *   k    bf16 [B][m][Hkv][d]
+ *   v    bf16 [B][m][Hkv][dv]
+ *   o    bf16 [B][n][H][dv]      written
+ *   lse  fp32 [B][H][n]          written (may be NULL: not written)
+ *   scale  multiplies Q K^T; must be positive and finite (pass 1/sqrt(d)
+ *          for the usual attention)
+ *   causal 0 or 1 (1 requires n == m)
+ * Supported: d == dv, d in {64, 128}; pointers 16-byte aligned; n, m >= 0.
+ * Computes S = Q K^T and P V on the tcgen05 tensor cores (bf16 operands,
+ * fp32 accumulation in tensor memory); P is rounded to bf16 before P V.
+ */
+fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int H, int Hkv, int n, int m, int d, int dv,
+                     float scale, int causal, void* stream);
+
+/*
+ * fa_forward_f32 — fp32 attention forward, dense batch; same shapes, layouts
+ * and semantics as fa_forward with every tensor in float32.  Arithmetic is
+ * IEEE fp32 on the CUDA cores (no TF32); each score is carried as a
+ * compensated (hi, lo) pair so that exp(s - m) keeps fp32 relative accuracy
+ * when the scores are in the hundreds.
+ * Supported: d, dv in {64, 128}; pointers 16-byte aligned.
+ */
+fa_status fa_forward_f32(const float* q, const float* k, const float* v, float* o, float* lse,
+                         int B, int H, int Hkv, int n, int m, int d, int dv,
+                         float scale, int causal, void* stream);
+
+/*
+ * fa_forward_varlen — bf16 attention forward over packed sequences of
+ * different lengths.  Sequence s owns query tokens [cu_seqlens_q[s],
+ * cu_seqlens_q[s+1]) and key tokens [cu_seqlens_k[s], cu_seqlens_k[s+1]).
+ *
+ *   q    bf16 [total_q][H][d],  k bf16 [total_k][Hkv][d],  v bf16 [total_k][Hkv][dv]
+ *   o    bf16 [total_q][H][dv]  written
+ *   lse  fp32 [H][total_q] written (may be NULL)
+ *   cu_seqlens_q, cu_seqlens_k  int32 [num_seqs + 1], DEVICE pointers,
+ *        non-decreasing, starting at 0, ending at total_q / total_k
+ *   total_q, total_k  rows of the packed q (and o) and k/v buffers; the
+ *        kernels never read or write a row outside them (a sequence whose
+ *        offsets exceed them is skipped and sets FA_ERR_INVALID_ARG in the
+ *        device status word)
+ *   max_seqlen_q, max_seqlen_k  upper bounds of the per-sequence lengths
+ *        (sizes the launch grid; a larger value only launches idle blocks)
+ * Supported as fa_forward; causal needs equal q and k lengths per sequence
+ * (the call cannot check this on the host; unequal lengths give the
+ * top-left-aligned mask).
+ */
+fa_status fa_forward_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                            const int* cu_seqlens_q, const int* cu_seqlens_k, int num_seqs,
+                            int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+                            int H, int Hkv, int d, int dv, float scale, int causal, void* stream);
+
+/*
+ * fa_paged_decode_workspace_size — bytes of workspace fa_paged_decode needs:
+ * the per-split partial triples (m, l: fp32 [num_seqs][H][num_splits] each;
+ * o: fp32 [num_seqs][H][num_splits][dv]), each array 256-byte aligned.
+ * Returns 0 on invalid sizes.
+ */
+size_t fa_paged_decode_workspace_size(int num_seqs, int H, int dv, int num_splits);
+
+/*
+ * fa_paged_decode — one query token per sequence against a paged KV cache,
+ * split-KV ("flash-decoding"), grouped heads.
+ * Passage: "S12 FlashAttention", 实现 (walk the block table; logical page p
+ * holds min(page_size, seq_len - p*page_size) valid tokens), 组合 (block
+ * table + grouped-head sharing + (m, l, o) in one loop), 它还解锁了什么 and
+ * 练习 1 (split the keys across blocks, merge the (m, l, o) triples).
+ *
+ *   q            bf16 [num_seqs][H][d]
+ *   k_cache      bf16 [num_pages][Hkv][page_size][d]
+ *   v_cache      bf16 [num_pages][Hkv][page_size][dv]
+ *   block_table  int32 [num_seqs][max_blocks_per_seq]: logical -> physical page
+ *   seq_lens     int32 [num_seqs], 0 <= seq_lens[s] <= max_blocks_per_seq*page_size
+ *   o            bf16 [num_seqs][H][dv]  written
+ *   lse          fp32 [num_seqs][H]      written (may be NULL)
+ *   num_splits   1..64: split x of a sequence with P pages covers logical
+ *                pages [ceil(x*P/X), ceil((x+1)*P/X)); empty splits are allowed
+ *   workspace    device scratch of at least fa_paged_decode_workspace_size()
+ *                bytes, 256-byte aligned; the call writes the partials there
+ *                and then merges them (fa_split_combine) on the same stream.
+ * Tokens past seq_len in the last page are never used (their cache contents
+ * may be anything, NaN included).  Page ids are range-checked on the device:
+ * an id outside [0, num_pages) is skipped and sets FA_ERR_BAD_BLOCK_TABLE.
+ * Supported: d == dv == 128, page_size == 16, H / Hkv <= 16.
+ */
+fa_status fa_paged_decode(const void* q, const void* k_cache, const void* v_cache,
+                          const int* block_table, const int* seq_lens, void* o, float* lse,
+                          int num_seqs, int H, int Hkv, int d, int dv, int page_size,
+                          int num_pages, int max_blocks_per_seq, int num_splits, float scale,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * fa_split_combine — merge per-split partial triples with the recurrence's
+ * rescale rule ("S12 FlashAttention", 练习 1): for each (s, h)
+ *     M = max_x m_x,  w_x = exp(m_x - M)  (w_x = 0 when m_x = -inf),
+ *     l = sum_x w_x l_x,  O = sum_x w_x o_x / l,  LSE = M + ln l.
+ *
+ *   part_m, part_l  fp32 [num_seqs][H][num_splits]: m_x is the split's maximum
+ *                   scaled score (natural units), l_x = sum exp(s_j - m_x)
+ *   part_o          fp32 [num_seqs][H][num_splits][dv]: sum exp(s_j - m_x) V[j]
+ *   o               bf16 [num_seqs][H][dv] written
+ *   lse             fp32 [num_seqs][H] written (may be NULL)
+ * An (s, h) whose splits are all empty gets O = 0 and LSE = -inf.
+ * Supported: dv % 4 == 0, dv <= 256, 1 <= num_splits <= 64.
+ */
+fa_status fa_split_combine(const float* part_m, const float* part_l, const float* part_o,
+                           void* o, float* lse, int num_seqs, int H, int num_splits, int dv,
+                           void* stream);
+
+/*
+ * fa_last_error — NUL-terminated description of the last non-OK status
+ * returned on the calling thread ("" if none).  Owned by the library; valid
+ * until the thread's next failing call.
+ */
+const char* fa_last_error(void);
+
+/*
+ * fa_get_device_status — synchronise `stream`, then read and clear the
+ * device status word of the current device (FA_OK, FA_ERR_TIMEOUT,
+ * FA_ERR_BAD_BLOCK_TABLE, or FA_ERR_INVALID_ARG for varlen offsets outside
+ * the buffers) into *status.  Returns FA_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+fa_status fa_get_device_status(void* stream, int* status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,177 @@
+"""GPU parity of the bf16 tcgen05 forward (fa_forward, fa_forward_varlen).
+
+Against the float64 oracle run on the same bf16-rounded inputs: O max-abs
+2e-2 and mean-abs 2e-3, LSE max-abs 1e-3.  Small cases compare every output;
+the full-size workloads compare sampled rows that cover every query tile,
+tile boundaries and the causal diagonal, in the launch configuration the
+bench times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tiled_online_softmax_sm_gb300 import binding as fb
+from tiled_online_softmax_sm_gb300 import inputs as I
+
+from _helpers import BF16_MAX_ABS, BF16_MEAN_ABS, assert_close, assert_lse_close, dev, dev_i32, host
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu(case):
+    return fb.forward(dev(case.q), dev(case.k), dev(case.v), case.scale, case.causal)
+
+
+def _check_full(case):
+    o, lse = _gpu(case)
+    o_ref, lse_ref = oracle.attention(case.q.values, case.k.values, case.v.values, case.scale,
+                                      case.causal)
+    assert_close(host(o), o_ref, BF16_MAX_ABS, BF16_MEAN_ABS, what=case.name)
+    assert_lse_close(host(lse), lse_ref, what=case.name)
+    assert fb.fa_get_device_status() == 0
+
+
+def _sample_rows(B, H, n, per_bh, seed):
+    """Rows (b, h, i): tile starts/ends, the diagonal neighbourhood and a
+    strided sweep with a per-(b, h) offset, so every 128-row tile is hit."""
+    g = I.rng(seed, 77)
+    rows = []
+    fixed = sorted({0, 1, 126, 127, 128, 129, 255, 256, n // 2, n - 129, n - 128, n - 2, n - 1})
+    fixed = [i for i in fixed if 0 <= i < n]
+    for b in range(B):
+        for h in range(H):
+            stride = max(1, n // per_bh)
+            off = int(g.integers(0, stride))
+            idx = set(range(off, n, stride)) | set(fixed)
+            rows.extend((b, h, i) for i in sorted(idx))
+    return np.array(rows, np.int32)
+
+
+def _check_rows(case, o, lse, rows):
+    o_ref, lse_ref = oracle.attention_rows(case.q.values, case.k.values, case.v.values, case.scale,
+                                           case.causal, rows)
+    oh = host(o)
+    lh = host(lse)
+    got_o = oh[rows[:, 0], rows[:, 2], rows[:, 1]]
+    got_l = lh[rows[:, 0], rows[:, 1], rows[:, 2]]
+    assert_close(got_o, o_ref, BF16_MAX_ABS, BF16_MEAN_ABS, what=case.name)
+    assert_lse_close(got_l, lse_ref, what=case.name)
+
+
+@pytest.mark.parametrize("shape", [
+    # B, H, Hkv, n, m, d, causal
+    (1, 2, 1, 300, 300, 128, True),
+    (2, 3, 3, 517, 517, 64, True),
+    (1, 2, 2, 200, 777, 128, False),
+    (1, 1, 1, 1, 1, 128, False),
+    (1, 1, 1, 1, 1, 64, True),
+    (2, 4, 2, 256, 256, 128, False),
+    (1, 2, 1, 129, 129, 64, False),
+    (1, 2, 2, 384, 384, 128, True),
+    (3, 2, 1, 640, 100, 64, False),
+])
+def test_small_shapes(shape):
+    B, H, Hkv, n, m, d, causal = shape
+    _check_full(I.dense_case(31, B, H, n, m, d, Hkv=Hkv, causal=causal, name=f"bf16_{shape}"))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_hot_x10(causal):
+    _check_full(I.dense_case(32, 1, 2, 640, 640, 128, causal=causal, hot=10.0, name="hot"))
+
+
+def test_no_keys_gives_zero_and_neg_inf():
+    q = torch.randn(1, 5, 2, 128, device="cuda").bfloat16()
+    k = torch.empty(1, 0, 2, 128, device="cuda").bfloat16()
+    o, lse = fb.forward(q, k, k, 0.088, False)
+    assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
+
+
+@pytest.mark.parametrize("variant", ["full", "causal", "hot"])
+def test_c2_full_size_sampled(variant):
+    """Batched prefill bf16: B=4, H=16, n=m=2048, d=dv=128 (non-causal, causal, x10 hot)."""
+    case = I.c2_bf16(causal=variant == "causal", hot=variant == "hot")
+    o, lse = _gpu(case)
+    rows = _sample_rows(4, 16, 2048, 64, 1)
+    _check_rows(case, o, lse, rows)
+    assert fb.fa_get_device_status() == 0
+
+
+def test_c3_full_size_sampled():
+    """Long-context causal prefill bf16: B=1, H=32, n=m=8192, d=dv=128."""
+    case = I.c3_bf16()
+    o, lse = _gpu(case)
+    rows = _sample_rows(1, 32, 8192, 96, 2)
+    _check_rows(case, o, lse, rows)
+    assert torch.isfinite(o.float()).all()
+    assert fb.fa_get_device_status() == 0
+
+
+# ----------------------------------------------------------------- varlen
+def _varlen_gpu(case):
+    T = int(case.cu_seqlens[-1])
+    cu = dev_i32(case.cu_seqlens)
+    mx = int(case.lens.max()) if len(case.lens) else 0
+    return fb.forward_varlen(dev(case.q), dev(case.k), dev(case.v), cu, cu, mx, mx, case.scale,
+                             case.causal)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_varlen_small_full(d):
+    lens = [1, 2, 127, 128, 129, 255, 256, 257, 5, 300]
+    case = I.varlen_case(41, lens, H=4, d=d, Hkv=2)
+    o, lse = _varlen_gpu(case)
+    o_ref, lse_ref = oracle.varlen(case.q.values, case.k.values, case.v.values, case.cu_seqlens,
+                                   case.cu_seqlens, case.scale, True)
+    assert_close(host(o), o_ref, BF16_MAX_ABS, BF16_MEAN_ABS, what=f"varlen d={d}")
+    assert_lse_close(host(lse), lse_ref, what=f"varlen d={d}")
+    assert fb.fa_get_device_status() == 0
+
+
+def test_varlen_noncausal_and_empty_sequence():
+    lens = [40, 0, 200]
+    case = I.varlen_case(42, lens, H=2, d=128, causal=False)
+    o, lse = _varlen_gpu(case)
+    o_ref, lse_ref = oracle.varlen(case.q.values, case.k.values, case.v.values, case.cu_seqlens,
+                                   case.cu_seqlens, case.scale, False)
+    assert_close(host(o), o_ref, BF16_MAX_ABS, BF16_MEAN_ABS)
+    assert_lse_close(host(lse), lse_ref)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_c5_varlen_full_size_sampled(d):
+    """Ragged causal varlen: 16 sequences, lengths uniform on [1, 4096], H=16,
+    10% of Q and K rows x20; sampled rows of every sequence and head."""
+    case = I.c5_varlen(d)
+    o, lse = _varlen_gpu(case)
+    oh, lh = host(o), host(lse)
+    g = I.rng(43, d)
+    for s in range(len(case.lens)):
+        a, b = int(case.cu_seqlens[s]), int(case.cu_seqlens[s + 1])
+        L = b - a
+        if L == 0:
+            continue
+        qs = case.q.values[a:b][None]
+        ks = case.k.values[a:b][None]
+        vs = case.v.values[a:b][None]
+        pick = sorted(set([0, L - 1, min(L - 1, 127), min(L - 1, 128)]) |
+                      set(g.integers(0, L, size=min(L, 24)).tolist()))
+        rows = np.array([(0, h, i) for h in range(case.H) for i in pick], np.int32)
+        o_ref, l_ref = oracle.attention_rows(qs, ks, vs, case.scale, True, rows)
+        got_o = oh[a + rows[:, 2], rows[:, 1]]
+        got_l = lh[rows[:, 1], a + rows[:, 2]]
+        assert_close(got_o, o_ref, BF16_MAX_ABS, BF16_MEAN_ABS, what=f"c5 d={d} seq {s}")
+        assert_lse_close(got_l, l_ref, what=f"c5 d={d} seq {s}")
+    assert fb.fa_get_device_status() == 0
+
+
+def test_varlen_offsets_outside_buffers_are_rejected_on_device():
+    case = I.varlen_case(44, [10, 20], H=2, d=64)
+    cu_bad = case.cu_seqlens.copy()
+    cu_bad[-1] = 999                     # past the 30 rows of the buffers
+    q, k, v = dev(case.q), dev(case.k), dev(case.v)
+    o = torch.zeros((30, 2, 64), dtype=torch.bfloat16, device="cuda")
+    fb.fa_forward_varlen(q, k, v, o, None, dev_i32(cu_bad), dev_i32(cu_bad), 2, 30, 30, 999, 999,
+                         2, 2, 64, 64, case.scale, 1)
+    assert fb.fa_get_device_status() == fb.FA_ERR_INVALID_ARG

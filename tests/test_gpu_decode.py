@@ -1,0 +1,155 @@
+"""GPU parity of the paged grouped-head split-KV decode and of the split merge.
+
+Against the float64 oracle: O max-abs 2e-2 and mean-abs 2e-3, LSE 1e-3.
+Block-table indexing is checked bit-exactly: the same kernel on the same KV
+laid out contiguously behind an identity table must give identical bits.
+Unused pool pages and the tail slots of each last page hold NaN, so a stray
+read shows up as NaN in O.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tiled_online_softmax_sm_gb300 import binding as fb
+from tiled_online_softmax_sm_gb300 import inputs as I
+
+from _helpers import BF16_MAX_ABS, BF16_MEAN_ABS, assert_close, assert_lse_close, dev, dev_i32, host
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu_decode(case, splits, workspace=None):
+    return fb.paged_decode(dev(case.q), dev(case.k_cache), dev(case.v_cache),
+                           dev_i32(case.block_table), dev_i32(case.seq_lens), splits, case.scale,
+                           workspace=workspace)
+
+
+def _oracle(case):
+    return oracle.paged_decode(case.q.values, case.k_cache.values, case.v_cache.values,
+                               case.block_table, case.seq_lens, case.scale)
+
+
+@pytest.mark.parametrize("splits", [1, 3, 4, 8, 16])
+def test_decode_small_ragged(splits):
+    # lengths: empty, 1 token, partial pages, exact pages, many pages
+    lens = [0, 1, 15, 16, 17, 100, 257, 640]
+    case = I.decode_case(5, num_seqs=len(lens), H=32, Hkv=8, d=128, lens=lens, max_blocks=48)
+    o, lse = _gpu_decode(case, splits)
+    o_ref, lse_ref = _oracle(case)
+    assert_close(host(o), o_ref, BF16_MAX_ABS, BF16_MEAN_ABS, what=f"decode X={splits}")
+    assert_lse_close(host(lse), lse_ref, what=f"decode lse X={splits}")
+    assert fb.fa_get_device_status() == 0
+
+
+@pytest.mark.parametrize("group", [1, 2, 4, 8, 16])
+def test_decode_group_sizes(group):
+    Hkv = 2
+    case = I.decode_case(6, num_seqs=3, H=Hkv * group, Hkv=Hkv, d=128, lens=[33, 200, 511],
+                         max_blocks=40)
+    o, lse = _gpu_decode(case, 4)
+    o_ref, lse_ref = _oracle(case)
+    assert_close(host(o), o_ref, BF16_MAX_ABS, BF16_MEAN_ABS, what=f"group {group}")
+    assert_lse_close(host(lse), lse_ref)
+
+
+def test_decode_partials_match_oracle_partials():
+    case = I.decode_case(8, num_seqs=4, H=8, Hkv=2, d=128, lens=[5, 64, 300, 129], max_blocks=24)
+    X = 5
+    need = fb.fa_paged_decode_workspace_size(4, 8, 128, X)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    _gpu_decode(case, X, workspace=ws)
+    torch.cuda.synchronize()
+    pm, pl, po = (host(t) for t in fb.decode_workspace_views(ws, 4, 8, 128, X))
+    rm, rl, ro = oracle.decode_partials(case.q.values, case.k_cache.values, case.v_cache.values,
+                                        case.block_table, case.seq_lens, X, case.scale)
+    assert np.array_equal(np.isneginf(pm), np.isneginf(rm))
+    fin = ~np.isneginf(rm)
+    assert np.abs(pm[fin] - rm[fin]).max() < 1e-3
+    # l and o are relative to each side's own m: compare after normalising
+    assert np.abs(pl[fin] * np.exp(pm[fin] - rm[fin]) - rl[fin]).max() / rl[fin].max() < 2e-2
+    on = po[fin] / pl[fin][:, None]
+    rn = ro[fin] / rl[fin][:, None]
+    assert np.abs(on - rn).max() < BF16_MAX_ABS
+    assert np.all(pl[~fin] == 0) and np.all(po[~fin] == 0)
+
+
+def test_block_table_bit_exact_vs_contiguous_layout():
+    """Same kernel, same arithmetic: a random permutation table and an identity
+    table over the same KV re-laid-out contiguously give identical bits."""
+    case = I.decode_case(9, num_seqs=6, H=32, Hkv=8, d=128, lens=[3, 40, 77, 512, 1000, 1500],
+                         max_blocks=100)
+    o1, l1 = _gpu_decode(case, 4)
+    # re-lay-out: sequence s's pages become consecutive physical pages
+    used = [case.block_table[s, :(int(L) + 15) // 16] for s, L in enumerate(case.seq_lens)]
+    order = np.concatenate(used)
+    P = len(order)
+    table = np.full_like(case.block_table, -1)
+    off = 0
+    for s, ids in enumerate(used):
+        table[s, :len(ids)] = np.arange(off, off + len(ids))
+        off += len(ids)
+    kc = I.Tensor("bf16", np.ascontiguousarray(case.k_cache.data[order]), None)
+    vc = I.Tensor("bf16", np.ascontiguousarray(case.v_cache.data[order]), None)
+    o2, l2 = fb.paged_decode(dev(case.q), dev(kc), dev(vc), dev_i32(table), dev_i32(case.seq_lens),
+                             4, case.scale)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1.view(torch.int32), l2.view(torch.int32))
+    assert P > 0
+
+
+def test_bad_block_id_sets_status_without_fault():
+    case = I.decode_case(10, num_seqs=2, H=8, Hkv=2, d=128, lens=[40, 40], max_blocks=4)
+    table = case.block_table.copy()
+    table[1, 1] = case.num_pages + 7      # out of range
+    o, lse = fb.paged_decode(dev(case.q), dev(case.k_cache), dev(case.v_cache), dev_i32(table),
+                             dev_i32(case.seq_lens), 2, case.scale)
+    assert fb.fa_get_device_status() == fb.FA_ERR_BAD_BLOCK_TABLE
+    assert fb.fa_get_device_status() == 0  # read clears it
+    # the untouched sequence is still right
+    o_ref, _ = _oracle(case)
+    assert_close(host(o)[0], o_ref[0], BF16_MAX_ABS, BF16_MEAN_ABS)
+
+
+def test_split_combine_against_oracle_merge():
+    rng = I.rng(11)
+    S, H, X, dv = 3, 4, 6, 128
+    pm = rng.normal(size=(S, H, X)) * 5
+    pm[0, 0, :] = -np.inf                  # all empty
+    pm[1, 2, ::2] = -np.inf                # some empty
+    pl = np.where(np.isneginf(pm), 0.0, rng.uniform(0.5, 50, size=(S, H, X)))
+    po = rng.normal(size=(S, H, X, dv)) * pl[..., None]
+    po[np.isneginf(pm)] = 0.0
+    pm32, pl32, po32 = (x.astype(np.float32) for x in (pm, pl, po))
+    o, lse = fb.split_combine(torch.from_numpy(pm32).cuda(), torch.from_numpy(pl32).cuda(),
+                              torch.from_numpy(po32).cuda())
+    o_ref, lse_ref = oracle.split_combine(pm32, pl32, po32)
+    assert_close(host(o), o_ref, BF16_MAX_ABS, BF16_MEAN_ABS)
+    assert_lse_close(host(lse), lse_ref)
+
+
+@pytest.mark.parametrize("splits", [4, 8, 16])
+def test_c4_full_size(splits):
+    """64 sequences, H=32, Hkv=8, d=128, page 16, lengths uniform on [512, 8192],
+    block tables random slices of a shared pool, split into 4/8/16 chunks."""
+    case = _c4()
+    o, lse = _gpu_decode(case, splits)
+    o_ref, lse_ref = _c4_ref()
+    assert_close(host(o), o_ref, BF16_MAX_ABS, BF16_MEAN_ABS, what=f"c4 X={splits}")
+    assert_lse_close(host(lse), lse_ref)
+    assert fb.fa_get_device_status() == 0
+
+
+_cache = {}
+
+
+def _c4():
+    if "case" not in _cache:
+        _cache["case"] = I.c4_decode()
+    return _cache["case"]
+
+
+def _c4_ref():
+    if "ref" not in _cache:
+        _cache["ref"] = _oracle(_c4())
+    return _cache["ref"]

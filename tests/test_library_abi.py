@@ -1,0 +1,121 @@
+"""CPU checks of the C ABI: the library loads, exports every entry point that
+include/fa.h declares, and rejects bad arguments before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tiled_online_softmax_sm_gb300 import binding as fb
+from tiled_online_softmax_sm_gb300 import build as fbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fbuild.build()
+    return fb.load()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "fa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_documented_entry_points():
+    assert _declared() == sorted(fb.EXPORTED)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def _fwd(lib, **kw):
+    args = dict(q=16, k=16, v=16, o=16, lse=16, B=1, H=2, Hkv=1, n=8, m=8, d=128, dv=128,
+                scale=0.1, causal=0)
+    args.update(kw)
+    return lib.fa_forward(args["q"], args["k"], args["v"], args["o"], args["lse"], args["B"],
+                          args["H"], args["Hkv"], args["n"], args["m"], args["d"], args["dv"],
+                          args["scale"], args["causal"], None)
+
+
+def test_forward_validation(lib):
+    assert _fwd(lib, H=3, Hkv=2) == fb.FA_ERR_INVALID_ARG
+    assert _fwd(lib, n=-1) == fb.FA_ERR_INVALID_ARG
+    assert _fwd(lib, q=None) == fb.FA_ERR_INVALID_ARG
+    assert _fwd(lib, q=8) == fb.FA_ERR_INVALID_ARG        # misaligned
+    assert _fwd(lib, causal=2) == fb.FA_ERR_INVALID_ARG
+    assert _fwd(lib, d=96, dv=96) == fb.FA_ERR_UNSUPPORTED
+    assert _fwd(lib, d=128, dv=64) == fb.FA_ERR_UNSUPPORTED
+    assert _fwd(lib, causal=1, n=8, m=9) == fb.FA_ERR_UNSUPPORTED
+    assert "causal" in fb.fa_last_error()
+    assert _fwd(lib, scale=0.0) == fb.FA_ERR_INVALID_ARG
+    assert _fwd(lib, scale=-1.0) == fb.FA_ERR_INVALID_ARG
+    assert _fwd(lib, B=0) == fb.FA_OK                     # nothing to do: no launch
+    assert _fwd(lib, n=0) == fb.FA_OK
+
+
+def test_forward_f32_and_varlen_validation(lib):
+    assert lib.fa_forward_f32(16, 16, 16, 16, 16, 1, 4, 3, 8, 8, 64, 64, 0.1, 0, None) == fb.FA_ERR_INVALID_ARG
+    assert lib.fa_forward_f32(16, 16, 16, 16, 16, 1, 4, 2, 8, 8, 32, 64, 0.1, 0, None) == fb.FA_ERR_UNSUPPORTED
+    assert lib.fa_forward_varlen(16, 16, 16, 16, 16, None, None, 2, 10, 10, 8, 8, 4, 4, 64, 64,
+                                 0.1, 1, None) == fb.FA_ERR_INVALID_ARG
+    assert lib.fa_forward_varlen(16, 16, 16, 16, 16, 16, 16, 2, 10, 10, 8, 8, 4, 4, 64, 128, 0.1,
+                                 1, None) == fb.FA_ERR_UNSUPPORTED
+    assert lib.fa_forward_varlen(16, 16, 16, 16, 16, 16, 16, 2, -1, 10, 8, 8, 4, 4, 64, 64, 0.1,
+                                 1, None) == fb.FA_ERR_INVALID_ARG
+    assert lib.fa_forward_varlen(16, 16, 16, 16, 16, 16, 16, 0, 0, 0, 0, 0, 4, 4, 64, 64, 0.1, 1,
+                                 None) == fb.FA_OK
+
+
+def test_decode_workspace_size(lib):
+    S, H, dv, X = 64, 32, 128, 16
+    tri = S * H * X
+    r = lambda x: (x + 255) // 256 * 256
+    assert fb.fa_paged_decode_workspace_size(S, H, dv, X) == 2 * r(tri * 4) + r(tri * dv * 4)
+    assert fb.fa_paged_decode_workspace_size(0, H, dv, X) == 0 + 0
+    assert fb.fa_paged_decode_workspace_size(S, 0, dv, X) == 0
+
+
+def _dec(lib, **kw):
+    a = dict(q=16, kc=16, vc=16, bt=16, sl=16, o=16, lse=16, S=4, H=32, Hkv=8, d=128, dv=128,
+             page=16, P=100, maxb=8, X=4, scale=0.1, ws=256, wsb=1 << 20)
+    a.update(kw)
+    return lib.fa_paged_decode(a["q"], a["kc"], a["vc"], a["bt"], a["sl"], a["o"], a["lse"], a["S"],
+                               a["H"], a["Hkv"], a["d"], a["dv"], a["page"], a["P"], a["maxb"],
+                               a["X"], a["scale"], a["ws"], a["wsb"], None)
+
+
+def test_decode_validation(lib):
+    assert _dec(lib, X=0) == fb.FA_ERR_INVALID_ARG
+    assert _dec(lib, X=65) == fb.FA_ERR_INVALID_ARG
+    assert _dec(lib, H=30) == fb.FA_ERR_INVALID_ARG
+    assert _dec(lib, page=32) == fb.FA_ERR_UNSUPPORTED
+    assert _dec(lib, d=64, dv=64) == fb.FA_ERR_UNSUPPORTED
+    assert _dec(lib, H=64, Hkv=2) == fb.FA_ERR_UNSUPPORTED       # group of 32 > 16
+    assert _dec(lib, ws=None) == fb.FA_ERR_WORKSPACE
+    assert _dec(lib, wsb=100) == fb.FA_ERR_WORKSPACE
+    assert _dec(lib, ws=272) == fb.FA_ERR_WORKSPACE            # not 256-byte aligned
+    assert _dec(lib, bt=None) == fb.FA_ERR_INVALID_ARG
+    assert _dec(lib, S=0) == fb.FA_OK
+
+
+def test_combine_validation(lib):
+    assert lib.fa_split_combine(16, 16, 16, 16, 16, 4, 8, 0, 128, None) == fb.FA_ERR_INVALID_ARG
+    assert lib.fa_split_combine(16, 16, 16, 16, 16, 4, 8, 4, 130, None) == fb.FA_ERR_UNSUPPORTED
+    assert lib.fa_split_combine(None, 16, 16, 16, 16, 4, 8, 4, 128, None) == fb.FA_ERR_INVALID_ARG
+    assert lib.fa_split_combine(16, 16, 16, 16, 16, 0, 8, 4, 128, None) == fb.FA_OK
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(fb.FaError):
+        fb._lib_saved = fb._lib
+        try:
+            fb._lib = None
+            fb.load(str(tmp_path / "nope.so"))
+        finally:
+            fb._lib = fb._lib_saved

@@ -1,0 +1,245 @@
+// C ABI of libfa_gb300.so: argument validation, workspace carving, the device
+// status word and error reporting.  Every entry point is declared and
+// documented in include/fa.h; the kernels live in the other translation units.
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+fa_status fail(fa_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+fa_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(FA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// One status word per device, in the library's own device memory: kernels
+// record timeouts and bad block-table ids there instead of faulting.
+__device__ int g_device_status = 0;
+
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices] = {nullptr};
+
+fa_status status_ptr(int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_device_status);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  *out = g_status_ptr[dev];
+  return FA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fa_status check_dense(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                      int B, int H, int Hkv, int n, int m, int d, int dv, int causal,
+                      const char* fn) {
+  if (B < 0 || n < 0 || m < 0) return fail(FA_ERR_INVALID_ARG, "%s: negative size", fn);
+  if (H <= 0 || Hkv <= 0 || H % Hkv != 0)
+    return fail(FA_ERR_INVALID_ARG, "%s: H=%d Hkv=%d (need H %% Hkv == 0)", fn, H, Hkv);
+  if (d <= 0 || dv <= 0) return fail(FA_ERR_INVALID_ARG, "%s: d=%d dv=%d", fn, d, dv);
+  if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "%s: causal=%d", fn, causal);
+  const bool empty_out = (B == 0 || n == 0);
+  if (!empty_out && (q == nullptr || o == nullptr))
+    return fail(FA_ERR_INVALID_ARG, "%s: null q/o", fn);
+  if (!empty_out && m > 0 && (k == nullptr || v == nullptr))
+    return fail(FA_ERR_INVALID_ARG, "%s: null k/v", fn);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(FA_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned (lse 4-byte)", fn);
+  if (causal && n != m)
+    return fail(FA_ERR_UNSUPPORTED, "%s: causal needs n == m (got n=%d m=%d)", fn, n, m);
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_last_error(void) { return g_err; }
+
+fa_status fa_get_device_status(void* stream, int* status) {
+  if (status == nullptr) return fail(FA_ERR_INVALID_ARG, "fa_get_device_status: null status");
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int* sp = nullptr;
+  fa_status st = status_ptr(&sp);
+  if (st != FA_OK) return st;
+  int value = 0;
+  e = cudaMemcpy(&value, sp, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read device status");
+  const int zero = 0;
+  e = cudaMemcpy(sp, &zero, sizeof(int), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "clear device status");
+  *status = value;
+  return FA_OK;
+}
+
+fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H, int Hkv, int n, int m, int d, int dv, float scale, int causal,
+                     void* stream) {
+  fa_status st = check_dense(q, k, v, o, lse, B, H, Hkv, n, m, d, dv, causal, "fa_forward");
+  if (st != FA_OK) return st;
+  if (!(scale > 0.f) || scale == INFINITY)
+    return fail(FA_ERR_INVALID_ARG, "fa_forward: scale must be positive and finite");
+  if (!(d == dv && (d == 64 || d == 128)))
+    return fail(FA_ERR_UNSUPPORTED, "fa_forward: d=%d dv=%d (supported: d == dv in {64, 128})", d,
+                dv);
+  if (B == 0 || n == 0) return FA_OK;
+  int* sp = nullptr;
+  if ((st = status_ptr(&sp)) != FA_OK) return st;
+  fa::FwdParams p{q, k, v, o, lse, nullptr, nullptr, B, H, Hkv, n, m, d, dv, 0, 0, scale, causal,
+                  sp};
+  const char* why = nullptr;
+  cudaError_t e = fa::launch_fwd_bf16(p, static_cast<cudaStream_t>(stream), &why);
+  if (e != cudaSuccess) return cuda_fail(e, why ? why : "fa_forward launch");
+  return FA_OK;
+}
+
+fa_status fa_forward_f32(const float* q, const float* k, const float* v, float* o, float* lse,
+                         int B, int H, int Hkv, int n, int m, int d, int dv, float scale,
+                         int causal, void* stream) {
+  fa_status st = check_dense(q, k, v, o, lse, B, H, Hkv, n, m, d, dv, causal, "fa_forward_f32");
+  if (st != FA_OK) return st;
+  if (!((d == 64 || d == 128) && (dv == 64 || dv == 128)))
+    return fail(FA_ERR_UNSUPPORTED, "fa_forward_f32: d=%d dv=%d (supported: 64, 128)", d, dv);
+  if (B == 0 || n == 0) return FA_OK;
+  int* sp = nullptr;
+  if ((st = status_ptr(&sp)) != FA_OK) return st;
+  fa::FwdParams p{q, k, v, o, lse, nullptr, nullptr, B, H, Hkv, n, m, d, dv, 0, 0, scale, causal,
+                  sp};
+  cudaError_t e = fa::launch_fwd_f32(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fa_forward_f32 launch");
+  return FA_OK;
+}
+
+fa_status fa_forward_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                            const int* cu_seqlens_q, const int* cu_seqlens_k, int num_seqs,
+                            int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int H,
+                            int Hkv, int d, int dv, float scale, int causal, void* stream) {
+  if (num_seqs < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || total_q < 0 || total_k < 0)
+    return fail(FA_ERR_INVALID_ARG, "fa_forward_varlen: negative size");
+  if (!(scale > 0.f) || scale == INFINITY)
+    return fail(FA_ERR_INVALID_ARG, "fa_forward_varlen: scale must be positive and finite");
+  if (num_seqs > 0 && (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr))
+    return fail(FA_ERR_INVALID_ARG, "fa_forward_varlen: null cu_seqlens");
+  fa_status st = check_dense(q, k, v, o, lse, num_seqs, H, Hkv, max_seqlen_q, max_seqlen_k, d, dv,
+                             0, "fa_forward_varlen");
+  if (st != FA_OK) return st;
+  if (causal != 0 && causal != 1)
+    return fail(FA_ERR_INVALID_ARG, "fa_forward_varlen: causal=%d", causal);
+  if (!(d == dv && (d == 64 || d == 128)))
+    return fail(FA_ERR_UNSUPPORTED, "fa_forward_varlen: d=%d dv=%d (supported: d == dv in {64, 128})",
+                d, dv);
+  if (num_seqs == 0 || max_seqlen_q == 0 || total_q == 0) return FA_OK;
+  int* sp = nullptr;
+  if ((st = status_ptr(&sp)) != FA_OK) return st;
+  fa::FwdParams p{q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, num_seqs, H, Hkv,
+                  max_seqlen_q, max_seqlen_k, d, dv, total_q, total_k, scale, causal, sp};
+  const char* why = nullptr;
+  cudaError_t e = fa::launch_fwd_bf16(p, static_cast<cudaStream_t>(stream), &why);
+  if (e != cudaSuccess) return cuda_fail(e, why ? why : "fa_forward_varlen launch");
+  return FA_OK;
+}
+
+static size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+size_t fa_paged_decode_workspace_size(int num_seqs, int H, int dv, int num_splits) {
+  if (num_seqs < 0 || H <= 0 || dv <= 0 || num_splits <= 0) return 0;
+  const size_t tri = (size_t)num_seqs * H * num_splits;
+  return 2 * round256(tri * sizeof(float)) + round256(tri * dv * sizeof(float));
+}
+
+fa_status fa_paged_decode(const void* q, const void* k_cache, const void* v_cache,
+                          const int* block_table, const int* seq_lens, void* o, float* lse,
+                          int num_seqs, int H, int Hkv, int d, int dv, int page_size,
+                          int num_pages, int max_blocks_per_seq, int num_splits, float scale,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  const char* fn = "fa_paged_decode";
+  if (num_seqs < 0 || num_pages < 0 || max_blocks_per_seq < 0)
+    return fail(FA_ERR_INVALID_ARG, "%s: negative size", fn);
+  if (H <= 0 || Hkv <= 0 || H % Hkv != 0)
+    return fail(FA_ERR_INVALID_ARG, "%s: H=%d Hkv=%d (need H %% Hkv == 0)", fn, H, Hkv);
+  if (num_splits < 1 || num_splits > 64)
+    return fail(FA_ERR_INVALID_ARG, "%s: num_splits=%d outside [1, 64]", fn, num_splits);
+  if (d != 128 || dv != 128)
+    return fail(FA_ERR_UNSUPPORTED, "%s: d=%d dv=%d (supported: 128)", fn, d, dv);
+  if (page_size != 16) return fail(FA_ERR_UNSUPPORTED, "%s: page_size=%d (supported: 16)", fn, page_size);
+  if (H / Hkv > 16) return fail(FA_ERR_UNSUPPORTED, "%s: H/Hkv=%d > 16", fn, H / Hkv);
+  if (num_seqs == 0) return FA_OK;
+  if (q == nullptr || o == nullptr || block_table == nullptr || seq_lens == nullptr ||
+      k_cache == nullptr || v_cache == nullptr)
+    return fail(FA_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (num_pages == 0 || max_blocks_per_seq == 0)
+    return fail(FA_ERR_INVALID_ARG, "%s: empty page pool or block table", fn);
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(block_table) & 3u) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return fail(FA_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
+  const size_t need = fa_paged_decode_workspace_size(num_seqs, H, dv, num_splits);
+  if (workspace == nullptr || workspace_bytes < need ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(FA_ERR_WORKSPACE, "%s: workspace %p of %zu bytes (need %zu, 256-byte aligned)", fn,
+                workspace, workspace_bytes, need);
+  int* sp = nullptr;
+  fa_status st = status_ptr(&sp);
+  if (st != FA_OK) return st;
+  const size_t tri = (size_t)num_seqs * H * num_splits;
+  char* ws = static_cast<char*>(workspace);
+  float* part_m = reinterpret_cast<float*>(ws);
+  float* part_l = reinterpret_cast<float*>(ws + round256(tri * sizeof(float)));
+  float* part_o = reinterpret_cast<float*>(ws + 2 * round256(tri * sizeof(float)));
+  fa::DecodeParams p{q, k_cache, v_cache, block_table, seq_lens, num_seqs, H, Hkv, d, dv,
+                     page_size, num_pages, max_blocks_per_seq, num_splits, scale,
+                     part_m, part_l, part_o, sp};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = fa::launch_decode_partials(p, s);
+  if (e != cudaSuccess) return cuda_fail(e, "fa_paged_decode partials launch");
+  fa::CombineParams c{part_m, part_l, part_o, o, lse, num_seqs, H, num_splits, dv};
+  e = fa::launch_split_combine(c, s);
+  if (e != cudaSuccess) return cuda_fail(e, "fa_paged_decode combine launch");
+  return FA_OK;
+}
+
+fa_status fa_split_combine(const float* part_m, const float* part_l, const float* part_o, void* o,
+                           float* lse, int num_seqs, int H, int num_splits, int dv, void* stream) {
+  const char* fn = "fa_split_combine";
+  if (num_seqs < 0 || H <= 0) return fail(FA_ERR_INVALID_ARG, "%s: bad sizes", fn);
+  if (num_splits < 1 || num_splits > 64)
+    return fail(FA_ERR_INVALID_ARG, "%s: num_splits=%d outside [1, 64]", fn, num_splits);
+  if (dv <= 0 || dv % 4 != 0 || dv > 256)
+    return fail(FA_ERR_UNSUPPORTED, "%s: dv=%d (need dv %% 4 == 0, dv <= 256)", fn, dv);
+  if (num_seqs == 0) return FA_OK;
+  if (part_m == nullptr || part_l == nullptr || part_o == nullptr || o == nullptr)
+    return fail(FA_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (!aligned16(part_o) || (reinterpret_cast<uintptr_t>(o) & 7u) ||
+      (reinterpret_cast<uintptr_t>(part_m) & 3u) || (reinterpret_cast<uintptr_t>(part_l) & 3u) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(FA_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
+  fa::CombineParams c{part_m, part_l, part_o, o, lse, num_seqs, H, num_splits, dv};
+  cudaError_t e = fa::launch_split_combine(c, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fa_split_combine launch");
+  return FA_OK;
+}
+
+}  // extern "C"

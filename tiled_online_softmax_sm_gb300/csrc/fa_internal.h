@@ -1,0 +1,59 @@
+// Internal launch interface between the C ABI layer (api.cu) and the kernel
+// translation units.  Host-side only; not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace fa {
+
+// Device status codes written by kernels (same values as fa_status).
+enum : int { kDevOk = 0, kDevInvalidArg = 1, kDevTimeout = 5, kDevBadBlockTable = 6 };
+
+// Forward problem.  Dense BSHD when cu_q == nullptr; otherwise packed varlen
+// (B = number of sequences, n/m = max lengths, token rows start at cu_q[b]).
+struct FwdParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;          // may be null
+  const int* cu_q;     // varlen only (device)
+  const int* cu_k;     // varlen only (device)
+  int B, H, Hkv, n, m, d, dv;
+  int total_q, total_k;  // varlen: rows of the packed q/k tensors (0 if unknown)
+  float scale;
+  int causal;
+  int* status;         // device status word
+};
+
+struct DecodeParams {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int* block_table;
+  const int* seq_lens;
+  int num_seqs, H, Hkv, d, dv, page_size, num_pages, max_blocks, num_splits;
+  float scale;
+  float* part_m;       // [S][H][X]
+  float* part_l;       // [S][H][X]
+  float* part_o;       // [S][H][X][dv]
+  int* status;
+};
+
+struct CombineParams {
+  const float* part_m;
+  const float* part_l;
+  const float* part_o;
+  void* o;             // bf16 [S][H][dv]
+  float* lse;          // [S][H], may be null
+  int num_seqs, H, num_splits, dv;
+};
+
+cudaError_t launch_fwd_f32(const FwdParams& p, cudaStream_t stream);
+cudaError_t launch_fwd_bf16(const FwdParams& p, cudaStream_t stream, const char** why);
+cudaError_t launch_decode_partials(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_split_combine(const CombineParams& p, cudaStream_t stream);
+
+}  // namespace fa

@@ -1,0 +1,226 @@
+// fp32 attention forward on the CUDA cores (IEEE fp32 arithmetic, no TF32).
+//
+// The online-softmax recurrence of "手搓 Attention" §7 (version 4) and
+// "S12 FlashAttention" (解法), one CTA per (batch, head, block of query rows):
+//   - the CTA keeps its query rows in registers and streams K/V tiles of
+//     kTileN rows through shared memory, one tile live at a time;
+//   - four threads share a query row; each owns a quarter of d (for Q·K) and a
+//     quarter of dv (for the accumulator), interleaved in float4 chunks so
+//     that the four lanes of a row read adjacent 16-byte words of a K/V row;
+//   - per tile: raw dot products q·k_j carried as compensated pairs, tile
+//     max, m_new, the rescale alpha = exp(scale·(m - m_new)) and
+//     p_j = exp(scale·(s_j - m_new)), both evaluated as 2^(x·log2 e); whole
+//     tiles above the causal diagonal are skipped and a fully masked tile uses
+//     0 as its reference (the -inf/NaN guard of "S12 FlashAttention", 实现).
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+constexpr int kRowsPerCta = 32;                 // query rows per CTA
+constexpr int kThreadsPerRow = 4;
+constexpr int kThreads = kRowsPerCta * kThreadsPerRow;  // 128
+constexpr int kTileN = 32;                      // keys per K/V tile
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Error-free transformations (Knuth's TwoSum; TwoProduct with one FMA) used
+// to carry each score as an unevaluated pair hi + lo.  With scores in the
+// hundreds a single fp32 score holds only ~1e-5 absolute precision, which the
+// weights exp(s - m) would inherit; the pair keeps s - m accurate to fp32
+// relative precision of the difference itself.  The __f*_rn intrinsics are
+// never contracted into FMAs, which would break the transformations.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float z = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, z)), __fsub_rn(b, z));
+}
+
+__device__ __forceinline__ void dot2_step(float a, float b, float& hi, float& lo) {
+  const float p = __fmul_rn(a, b);
+  const float r = fmaf(a, b, -p);  // exact: a*b = p + r
+  float s, e;
+  two_sum(hi, p, s, e);
+  hi = s;
+  lo = __fadd_rn(lo, __fadd_rn(e, r));
+}
+
+__device__ __forceinline__ void pair_add(float& hi, float& lo, float hi2, float lo2) {
+  float s, e;
+  two_sum(hi, hi2, s, e);
+  hi = s;
+  lo = __fadd_rn(__fadd_rn(lo, lo2), e);
+}
+
+// (a_hi + a_lo) - (b_hi + b_lo), scaled, in fp32
+__device__ __forceinline__ float pair_diff_scaled(float a_hi, float a_lo, float b_hi, float b_lo,
+                                                  float scale) {
+  return __fmul_rn(__fadd_rn(__fsub_rn(a_hi, b_hi), __fsub_rn(a_lo, b_lo)), scale);
+}
+
+template <int D, int DV>
+__global__ void __launch_bounds__(kThreads)
+fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
+               const float* __restrict__ v, float* __restrict__ o, float* __restrict__ lse,
+               int B, int H, int Hkv, int n, int m, float scale, int causal) {
+  extern __shared__ float4 smem4[];
+  float4* sK = smem4;                           // [kTileN][D/4]
+  float4* sV = smem4 + kTileN * (D / 4);        // [kTileN][DV/4]
+
+  const float scale_log2 = scale * kLog2e;
+  const int tid = threadIdx.x;
+  const int row = tid / kThreadsPerRow;
+  const int part = tid % kThreadsPerRow;
+  const int h = blockIdx.y;
+  const int b = blockIdx.z;
+  const int hk = h / (H / Hkv);
+  const int q0 = blockIdx.x * kRowsPerCta;
+  const int i = q0 + row;                       // query index of this row
+  const bool row_valid = i < n;
+
+  constexpr int QC = D / 16;    // float4 chunks of q owned by this thread
+  constexpr int VC = DV / 16;   // float4 chunks of acc owned by this thread
+
+  float4 qr[QC];
+  float4 acc[VC];
+  {
+    const float4* qrow = reinterpret_cast<const float4*>(q + (((size_t)b * n + (row_valid ? i : 0)) * H + h) * D);
+#pragma unroll
+    for (int c = 0; c < QC; ++c) qr[c] = row_valid ? qrow[c * 4 + part] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int c = 0; c < VC; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  // running maximum of the raw dot products, as a pair; -inf until a key is seen
+  float m_hi = -INFINITY, m_lo = 0.f;
+  float l_run = 0.f;
+
+  int kv_end = m;
+  if (causal) kv_end = min(m, q0 + kRowsPerCta);
+  const size_t k_row_stride = (size_t)Hkv * D;
+  const size_t v_row_stride = (size_t)Hkv * DV;
+  const float* kbase = k + ((size_t)b * m * Hkv + hk) * D;
+  const float* vbase = v + ((size_t)b * m * Hkv + hk) * DV;
+
+  for (int j0 = 0; j0 < kv_end; j0 += kTileN) {
+    const int cols = min(kTileN, m - j0);
+    __syncthreads();  // previous tile fully consumed
+    for (int idx = tid; idx < kTileN * (D / 4); idx += kThreads) {
+      int r = idx / (D / 4), c = idx % (D / 4);
+      sK[idx] = r < cols ? reinterpret_cast<const float4*>(kbase + (size_t)(j0 + r) * k_row_stride)[c]
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int idx = tid; idx < kTileN * (DV / 4); idx += kThreads) {
+      int r = idx / (DV / 4), c = idx % (DV / 4);
+      sV[idx] = r < cols ? reinterpret_cast<const float4*>(vbase + (size_t)(j0 + r) * v_row_stride)[c]
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __syncthreads();
+
+    int vis = cols;                 // visible keys of this row in the tile: [0, vis)
+    if (causal) vis = min(vis, i - j0 + 1);
+    if (!row_valid) vis = 0;
+
+    float s_hi[kTileN], s_lo[kTileN];
+    float t_hi = -INFINITY, t_lo = 0.f;   // tile maximum
+#pragma unroll
+    for (int j = 0; j < kTileN; ++j) {
+      const float4* kr = sK + j * (D / 4);
+      float hi = 0.f, lo = 0.f;
+#pragma unroll
+      for (int c = 0; c < QC; ++c) {
+        const float4 kk = kr[c * 4 + part];
+        dot2_step(qr[c].x, kk.x, hi, lo);
+        dot2_step(qr[c].y, kk.y, hi, lo);
+        dot2_step(qr[c].z, kk.z, hi, lo);
+        dot2_step(qr[c].w, kk.w, hi, lo);
+      }
+#pragma unroll
+      for (int off = 1; off < kThreadsPerRow; off <<= 1)
+        pair_add(hi, lo, __shfl_xor_sync(0xffffffffu, hi, off), __shfl_xor_sync(0xffffffffu, lo, off));
+      if (j >= vis) {
+        hi = -INFINITY;
+        lo = 0.f;
+      }
+      s_hi[j] = hi;
+      s_lo[j] = lo;
+      if (hi > t_hi) {
+        t_hi = hi;
+        t_lo = lo;
+      }
+    }
+    // m_new = max(m, tile max); reference 0 while nothing is visible (guard)
+    float n_hi = m_hi, n_lo = m_lo;
+    if (t_hi > n_hi) {
+      n_hi = t_hi;
+      n_lo = t_lo;
+    }
+    const bool empty = n_hi == -INFINITY;
+    const float r_hi = empty ? 0.f : n_hi, r_lo = empty ? 0.f : n_lo;
+    const float alpha = m_hi == -INFINITY ? 1.f : exp2f(pair_diff_scaled(m_hi, m_lo, r_hi, r_lo, scale_log2));
+#pragma unroll
+    for (int c = 0; c < VC; ++c) {
+      acc[c].x *= alpha; acc[c].y *= alpha; acc[c].z *= alpha; acc[c].w *= alpha;
+    }
+    float psum = 0.f;
+#pragma unroll
+    for (int j = 0; j < kTileN; ++j) {
+      const float p = s_hi[j] == -INFINITY ? 0.f
+                                           : exp2f(pair_diff_scaled(s_hi[j], s_lo[j], r_hi, r_lo, scale_log2));
+      psum += p;
+      const float4* vr = sV + j * (DV / 4);
+#pragma unroll
+      for (int c = 0; c < VC; ++c) {
+        const float4 vv = vr[c * 4 + part];
+        acc[c].x = fmaf(p, vv.x, acc[c].x);
+        acc[c].y = fmaf(p, vv.y, acc[c].y);
+        acc[c].z = fmaf(p, vv.z, acc[c].z);
+        acc[c].w = fmaf(p, vv.w, acc[c].w);
+      }
+    }
+    l_run = l_run * alpha + psum;
+    m_hi = n_hi;
+    m_lo = n_lo;
+  }
+
+  if (!row_valid) return;
+  const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+  float4* orow = reinterpret_cast<float4*>(o + (((size_t)b * n + i) * H + h) * DV);
+#pragma unroll
+  for (int c = 0; c < VC; ++c) {
+    const float4 x = acc[c];
+    orow[c * 4 + part] = make_float4(x.x * inv, x.y * inv, x.z * inv, x.w * inv);
+  }
+  if (lse != nullptr && part == 0)
+    lse[((size_t)b * H + h) * n + i] =
+        l_run > 0.f ? (m_hi + m_lo) * scale + logf(l_run) : -INFINITY;
+}
+
+template <int D, int DV>
+cudaError_t launch(const FwdParams& p, cudaStream_t stream) {
+  const size_t smem = sizeof(float) * kTileN * (D + DV);
+  cudaError_t e = cudaFuncSetAttribute(fwd_f32_kernel<D, DV>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((p.n + kRowsPerCta - 1) / kRowsPerCta, p.H, p.B);
+  fwd_f32_kernel<D, DV><<<grid, kThreads, smem, stream>>>(
+      static_cast<const float*>(p.q), static_cast<const float*>(p.k),
+      static_cast<const float*>(p.v), static_cast<float*>(p.o), p.lse, p.B, p.H, p.Hkv, p.n,
+      p.m, p.scale, p.causal);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_f32(const FwdParams& p, cudaStream_t stream) {
+  if (p.n == 0 || p.B == 0) return cudaSuccess;
+  if (p.d == 64 && p.dv == 64) return launch<64, 64>(p, stream);
+  if (p.d == 64 && p.dv == 128) return launch<64, 128>(p, stream);
+  if (p.d == 128 && p.dv == 64) return launch<128, 64>(p, stream);
+  if (p.d == 128 && p.dv == 128) return launch<128, 128>(p, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fa
