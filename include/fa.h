@@ -152,6 +152,37 @@ fa_status fa_paged_decode(const void* q, const void* k_cache, const void* v_cach
                           void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * fa_paged_decode_noalloc — fa_paged_decode for callers that cannot allocate.
+ * The pages have no counterpart for this call: it exists for library users.
+ *
+ * Some callers may not call cudaMalloc themselves: a plugin inside a host
+ * framework that owns all device memory through its own allocator, or a
+ * serving loop that must not allocate once it runs (cudaMalloc can
+ * synchronise the device).  This entry point computes exactly what
+ * fa_paged_decode computes (same kernels, same arguments minus the
+ * workspace) and keeps its split partials in one fixed device array of
+ * FA_NOALLOC_SCRATCH_BYTES that the library itself declares.  It allocates
+ * nothing; the caller still owns and passes every input and output.
+ *   - Every GPU that loads the library holds that array until the process ends.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - A problem whose partials (fa_paged_decode_workspace_size) exceed the
+ *     array is rejected with FA_ERR_WORKSPACE before anything is launched.
+ *   - All calls share the array, which keeps the last call's contents (every
+ *     partial the merge reads is rewritten, so nothing needs clearing).  Calls
+ *     that overlap on the GPU (other streams, other threads) race on it and
+ *     corrupt each other: serialise them.
+ * Arguments, layouts, supported sizes and device status as fa_paged_decode.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (16u << 20)
+fa_status fa_paged_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                  const int* block_table, const int* seq_lens, void* o,
+                                  float* lse, int num_seqs, int H, int Hkv, int d, int dv,
+                                  int page_size, int num_pages, int max_blocks_per_seq,
+                                  int num_splits, float scale, void* stream);
+
+/*
  * fa_split_combine — merge per-split partial triples with the recurrence's
  * rescale rule ("S12 FlashAttention", 练习 1): for each (s, h)
  *     M = max_x m_x,  w_x = exp(m_x - M)  (w_x = 0 when m_x = -inf),

@@ -29,7 +29,9 @@ FA_ERR_TIMEOUT = 5
 FA_ERR_BAD_BLOCK_TABLE = 6
 
 EXPORTED = ("fa_forward", "fa_forward_f32", "fa_forward_varlen", "fa_paged_decode_workspace_size",
-            "fa_paged_decode", "fa_split_combine", "fa_last_error", "fa_get_device_status")
+            "fa_paged_decode", "fa_paged_decode_noalloc", "fa_split_combine", "fa_last_error",
+            "fa_get_device_status")
+FA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class FaError(RuntimeError):
@@ -59,12 +61,13 @@ def load(path: str = LIB_PATH):
         lib.fa_paged_decode_workspace_size.argtypes = [I, I, I, I]
         lib.fa_paged_decode_workspace_size.restype = Z
         lib.fa_paged_decode.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, P, Z, P]
+        lib.fa_paged_decode_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, P]
         lib.fa_split_combine.argtypes = [P, P, P, P, P, I, I, I, I, P]
         lib.fa_last_error.argtypes = []
         lib.fa_last_error.restype = ctypes.c_char_p
         lib.fa_get_device_status.argtypes = [P, ctypes.POINTER(I)]
         for name in ("fa_forward", "fa_forward_f32", "fa_forward_varlen", "fa_paged_decode",
-                     "fa_split_combine", "fa_get_device_status"):
+                     "fa_paged_decode_noalloc", "fa_split_combine", "fa_get_device_status"):
             getattr(lib, name).restype = I
         _lib = lib
         return lib
@@ -124,6 +127,19 @@ def fa_paged_decode(q, k_cache, v_cache, block_table, seq_lens, o, lse, num_seqs
                                   _p(o), _p(lse), num_seqs, H, Hkv, d, dv, page_size, num_pages,
                                   max_blocks_per_seq, num_splits, float(scale), _p(workspace),
                                   int(workspace_bytes), _stream(stream)))
+
+
+def fa_paged_decode_noalloc(q, k_cache, v_cache, block_table, seq_lens, o, lse, num_seqs, H, Hkv,
+                            d, dv, page_size, num_pages, max_blocks_per_seq, num_splits, scale,
+                            stream=None):
+    """fa_paged_decode without a workspace: for callers that may not allocate
+    device memory themselves.  The split partials live in the library's own
+    fixed device array (FA_NOALLOC_SCRATCH_BYTES); calls share it, so calls
+    that overlap on the GPU must not be issued."""
+    _check(load().fa_paged_decode_noalloc(_p(q), _p(k_cache), _p(v_cache), _p(block_table),
+                                          _p(seq_lens), _p(o), _p(lse), num_seqs, H, Hkv, d, dv,
+                                          page_size, num_pages, max_blocks_per_seq, num_splits,
+                                          float(scale), _stream(stream)))
 
 
 def fa_split_combine(part_m, part_l, part_o, o, lse, num_seqs, H, num_splits, dv, stream=None):

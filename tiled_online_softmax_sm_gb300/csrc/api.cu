@@ -74,6 +74,12 @@ fa_status check_dense(const void* q, const void* k, const void* v, const void* o
 
 }  // namespace
 
+// Shared with the other C-ABI translation units (same error text and status word).
+namespace fa {
+fa_status api_fail(fa_status st, const char* msg) { return fail(st, "%s", msg); }
+fa_status api_status_ptr(int** out) { return status_ptr(out); }
+}  // namespace fa
+
 extern "C" {
 
 const char* fa_last_error(void) { return g_err; }
