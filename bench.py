@@ -66,6 +66,17 @@ def shard_units(total: int, rank: int, world: int) -> range:
     return range(lo, hi)
 
 
+def reduce_max(values, device=None):
+    """Element-wise max over ranks of a list of floats (identity without a
+    process group).  Used for the timed region: the slowest rank decides."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -217,12 +228,16 @@ def cpu_oracle_decode_sample(case, target_s: float = 4.0):
 
 
 # --------------------------------------------------------------- main arms
-def build_inputs(rank: int):
+def build_inputs(rank: int, world: int = 1):
+    """This rank's share of the global job: the job is `world` independent
+    copies of the per-GPU workload (forward batch + decode batch), each with
+    its own seed; rank r takes copy r (weak scaling)."""
     from tiled_online_softmax_sm_gb300 import inputs as I
-    fwd = I.dense_case(I.BASE_SEED + rank, FWD_SHAPE["B"], FWD_SHAPE["H"], FWD_SHAPE["n"],
+    (copy,) = shard_units(world, rank, world)
+    fwd = I.dense_case(I.BASE_SEED + copy, FWD_SHAPE["B"], FWD_SHAPE["H"], FWD_SHAPE["n"],
                        FWD_SHAPE["m"], FWD_SHAPE["d"], dtype="bf16", causal=True, stream=3,
                        name="c3")
-    dec = I.c4_decode(seed=I.BASE_SEED + rank)
+    dec = I.c4_decode(seed=I.BASE_SEED + copy)
     return fwd, dec
 
 
@@ -270,7 +285,7 @@ def run_ours(args, world, rank, local):
         dist.init_process_group("nccl", device_id=dev)
     fb.load()
 
-    fwd, dec = build_inputs(rank)
+    fwd, dec = build_inputs(rank, world)
 
     def to_dev(t):
         return torch.from_numpy(t.data.view(np.int16)).to(dev).view(torch.bfloat16)
@@ -343,10 +358,7 @@ def run_ours(args, world, rank, local):
         raise RuntimeError(f"device status {status} during the timed region")
 
     # max over ranks of the timed region and of each part
-    vals = torch.tensor([total_ms, sum(fwd_ms), sum(dec_ms)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    total_ms, fwd_sum, dec_sum = (float(x) for x in vals.cpu())
+    total_ms, fwd_sum, dec_sum = reduce_max([total_ms, sum(fwd_ms), sum(dec_ms)], device=dev)
 
     flops = fwd_flops(**FWD_SHAPE)
     fwd_tflops = flops * K * world / (fwd_sum / 1e3) / 1e12
