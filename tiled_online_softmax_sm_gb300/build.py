@@ -9,6 +9,7 @@ from __future__ import annotations
 import concurrent.futures as cf
 import glob
 import os
+import re
 import shutil
 import subprocess
 import sys
@@ -36,17 +37,41 @@ def _headers():
         glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
+# Kernels that re-split registers with setmaxnreg: the split is sized for
+# exactly this many registers per thread at launch (see the kernel source).
+REQUIRED_REGS = {"fwd_bf16_kernel": 168}
+
+
+def _check_regs(src: str, ptxas_log: str):
+    """Refuse an object whose setmaxnreg kernels were not compiled with the
+    register count their split assumes (a wrong split would stall forever)."""
+    current = None
+    for line in ptxas_log.splitlines():
+        m = re.search(r"Compiling entry function '([^']+)'", line)
+        if m:
+            current = m.group(1)
+            continue
+        m = re.search(r"Used (\d+) registers", line)
+        if m and current:
+            for name, regs in REQUIRED_REGS.items():
+                if name in current and int(m.group(1)) != regs:
+                    raise RuntimeError(f"{src}: {name} uses {m.group(1)} registers, its "
+                                       f"setmaxnreg split assumes {regs}")
+            current = None
+
+
 def _compile(src: str, verbose: bool) -> str:
     obj = os.path.join(BUILD, os.path.basename(src).replace(".cu", ".o"))
     newest = max([os.path.getmtime(src)] + [os.path.getmtime(h) for h in _headers()])
     if os.path.exists(obj) and os.path.getmtime(obj) >= newest:
         return obj
-    cmd = [nvcc()] + NVCC_FLAGS + (["-Xptxas", "-v"] if verbose else []) + ["-c", src, "-o", obj + ".tmp"]
+    cmd = [nvcc()] + NVCC_FLAGS + ["-Xptxas", "-v", "-c", src, "-o", obj + ".tmp"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
     if verbose and r.stderr:
         sys.stderr.write(r.stderr)
+    _check_regs(src, r.stderr)
     os.replace(obj + ".tmp", obj)
     return obj
 

@@ -5,14 +5,15 @@
 // 01" (a CTA owns query tiles and streams every K/V tile past them), mapped to
 // Blackwell:
 //
-//   CTA = two 128-row query tiles of one (batch, head), 10 warps:
+//   CTA = two 128-row query tiles of one (batch, head), 12 warps:
 //     warp 0      TMA producer: Q tiles once, then K(j), V(j) through a
 //                 kStages-slot shared-memory ring (128-byte swizzle)
 //     warp 1      owns the tensor memory (512 columns) and, on one lane,
 //                 issues every tcgen05.mma:
 //                   S_i = Q_i K(j)^T   (SS: both operands in shared memory)
 //                   O_i += P_i V(j)    (TS: P in tensor memory, V MN-major)
-//     warps 2-5   softmax for query tile 0, warps 6-9 for tile 1: thread =
+//     warps 2-3   idle (they complete the first warpgroup)
+//     warps 4-7   softmax for query tile 0, warps 8-11 for tile 1: thread =
 //                 one query row = one tensor-memory lane, so row max and row
 //                 sum need no shuffles.
 //   Tensor memory: S_0 | S_1 (128 fp32 columns each), O_0 | O_1 (d columns
@@ -50,7 +51,16 @@ namespace {
 
 constexpr int kBlockM = 128;   // query rows per tile (= tensor-memory lanes)
 constexpr int kBlockN = 128;   // keys per K/V tile
-constexpr int kThreads = 320;  // 10 warps
+constexpr int kThreads = 384;  // 12 warps = 3 warpgroups
+// Register split (setmaxnreg): the launch gives every thread kLaunchRegs; the
+// TMA/MMA warpgroup drops to kProducerRegs and the two softmax warpgroups rise
+// to kSoftmaxRegs.  128*(kProducerRegs + 2*kSoftmaxRegs) must not exceed
+// 384*kLaunchRegs, or the increase would wait forever; the build refuses a
+// library whose kernel does not use exactly kLaunchRegs registers.
+constexpr int kLaunchRegs = 168;
+constexpr int kProducerRegs = 72;
+constexpr int kSoftmaxRegs = 216;
+static_assert(128 * (kProducerRegs + 2 * kSoftmaxRegs) <= kThreads * kLaunchRegs, "register split");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -69,7 +79,7 @@ struct Cfg {
 struct Shared {
   uint64_t q_full[2];
   uint64_t s_full[2];
-  uint64_t p_full[2];
+  uint64_t p_full[4];   // [tile][half]
   uint64_t o_done[2];
   uint64_t kv_full[8];
   uint64_t kv_empty[8];
@@ -140,7 +150,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(bar_q + 8 * i, 1);
       ptx::mbar_init(bar_s + 8 * i, 1);
-      ptx::mbar_init(bar_p + 8 * i, kBlockM);
+      ptx::mbar_init(bar_p + 16 * i, kBlockM);
+      ptx::mbar_init(bar_p + 16 * i + 8, kBlockM);
       ptx::mbar_init(bar_o + 8 * i, 1);
     }
     for (int s = 0; s < C::kStages; ++s) {
@@ -161,6 +172,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   ptx::tc_fence_after();
   const uint32_t tbase = sh.tmem_base;
 
+  if (warp < 4) {
+  ptx::setmaxnreg_dec<kProducerRegs>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -221,14 +234,23 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           ptx::mma_ss(tbase + i * kBlockN, ad, bd, C::kIdescS, k > 0);
         }
       };
-      auto issue_pv = [&](int i, int slot, int j) {
+      // O_i += P_i V(j) in two halves of 64 keys, each issued once the softmax
+      // warps have stored that half of P; false if a wait failed
+      auto issue_pv = [&](int i, int slot, int j) -> bool {
         const uint32_t vaddr = ptx::smem_u32(sKV + slot * C::kTileBytes);
 #pragma unroll
-        for (int k = 0; k < kBlockN / 16; ++k) {
-          const uint64_t bd = ptx::smem_desc_sw128(vaddr + k * 2048, 16384, 1024);
-          ptx::mma_ts(tbase + 256 + i * D, tbase + i * kBlockN + k * 8, bd, C::kIdescO,
-                      (j > 0 || k > 0) ? 1u : 0u);
+        for (int hf = 0; hf < 2; ++hf) {
+          if (!ptx::mbar_wait(bar_p + 16 * i + 8 * hf, j & 1, status, abort_flag)) return false;
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kBlockN / 32; ++kk) {
+            const int k = hf * (kBlockN / 32) + kk;
+            const uint64_t bd = ptx::smem_desc_sw128(vaddr + k * 2048, 16384, 1024);
+            ptx::mma_ts(tbase + 256 + i * D, tbase + i * kBlockN + k * 8, bd, C::kIdescO,
+                        (j > 0 || k > 0) ? 1u : 0u);
+          }
         }
+        return true;
       };
       // prologue: S_i(0)
       if (ok && n_kv_max > 0) {
@@ -249,9 +271,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const bool has_next = j + 1 < n_kv_max;
         if (!(ok = ptx::mbar_wait(bar_kvf + 8 * sv, (lv / C::kStages) & 1, status, abort_flag))) break;
         if (j < n_kv[0]) {
-          if (!(ok = ptx::mbar_wait(bar_p, j & 1, status, abort_flag))) break;
-          ptx::tc_fence_after();
-          issue_pv(0, sv, j);
+          if (!(ok = issue_pv(0, sv, j))) break;
           if (j == n_kv[0] - 1) ptx::tc_commit(bar_o);
         }
         if (has_next) {
@@ -263,9 +283,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           ptx::tc_commit(bar_s);
         }
         if (j < n_kv[1]) {
-          if (!(ok = ptx::mbar_wait(bar_p + 8, j & 1, status, abort_flag))) break;
-          ptx::tc_fence_after();
-          issue_pv(1, sv, j);
+          if (!(ok = issue_pv(1, sv, j))) break;
           if (j == n_kv[1] - 1) ptx::tc_commit(bar_o + 8);
         }
         ptx::tc_commit(bar_kve + 8 * sv);  // V(j) slot
@@ -279,9 +297,11 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       ptx::tc_commit(bar_drain);
       ptx::mbar_wait(bar_drain, 0, nullptr);
     }
+  }
   } else {
+    ptx::setmaxnreg_inc<kSoftmaxRegs>();
     // ------------------------------------------------------------ softmax
-    const int i = (warp - 2) / 4;             // query tile of this warpgroup
+    const int i = (warp - 4) / 4;             // query tile of this warpgroup
     const int quarter = warp & 3;             // tensor-memory lane quarter
     const int r = quarter * 32 + lane;        // row in the tile
     const int q_start = q_start0 + i * kBlockM;
@@ -316,7 +336,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sr[c][e]));
+        for (int e = 0; e < 32; e += 2)
+          mx = ptx::fmax3(mx, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
       const float m_tile = mx * scale_log2;    // scale > 0: max commutes with it
       const bool raise = m_tile > m_ref + kRescaleThreshold || (m_ref == -INFINITY && m_tile > -INFINITY);
       float alpha = 1.f;
@@ -326,21 +347,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         l_run *= alpha;
       }
       const float ref = m_ref == -INFINITY ? 0.f : m_ref;
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t pr[2][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float p0 = ptx::ex2(fmaf(__uint_as_float(sr[c][e]), scale_log2, -ref));
-          const float p1 = ptx::ex2(fmaf(__uint_as_float(sr[c][e + 1]), scale_log2, -ref));
-          ls[c] += p0 + p1;
-          pr[c >> 1][(c & 1) * 16 + e / 2] = ptx::pack_bf16x2(p0, p1);
-        }
-      l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      ptx::tmem_st32(s_col, pr[0]);
-      ptx::tmem_st32(s_col + 32, pr[1]);
-      // rescale acc when this warp raised a reference after the first tile
+      // rescale acc first when this warp raised a reference after the first
+      // tile: no P V of this tile may run before it
       if (__any_sync(0xffffffffu, raise && j > 0 && alpha != 1.f)) {
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
@@ -352,9 +360,37 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           ptx::tmem_st32(o_col + c * 32, ov);
         }
       }
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar_p + 8 * i);
+      // p = 2^(s*scale*log2e - ref), two halves of 64 keys; each half is
+      // handed to the MMA warp as soon as it sits in tensor memory
+      const uint64_t sc2 = ptx::f2_bits(scale_log2, scale_log2);
+      const uint64_t nref2 = ptx::f2_bits(-ref, -ref);
+      uint64_t lsum2 = ptx::f2_bits(0.f, 0.f);
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t pr[32];
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = hf * 2 + cc;
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const uint64_t x = ptx::ffma2(
+                ptx::f2_bits(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])), sc2, nref2);
+            float x0, x1;
+            ptx::f2_split(x, x0, x1);
+            const float p0 = ptx::ex2(x0);
+            const float p1 = ptx::ex2(x1);
+            lsum2 = ptx::fadd2(lsum2, ptx::f2_bits(p0, p1));
+            pr[cc * 16 + e / 2] = ptx::pack_bf16x2(p0, p1);
+          }
+        }
+        ptx::tmem_st32(s_col + hf * 32, pr);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_p + 16 * i + 8 * hf);
+      }
+      float ls0, ls1;
+      ptx::f2_split(lsum2, ls0, ls1);
+      l_run += ls0 + ls1;
     }
 
     // ---- epilogue: O = acc / l (bf16), LSE = (ref + log2 l) ln 2
