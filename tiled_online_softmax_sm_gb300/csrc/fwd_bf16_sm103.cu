@@ -58,8 +58,8 @@ constexpr int kThreads = 384;  // 12 warps = 3 warpgroups
 // 384*kLaunchRegs, or the increase would wait forever; the build refuses a
 // library whose kernel does not use exactly kLaunchRegs registers.
 constexpr int kLaunchRegs = 168;
-constexpr int kProducerRegs = 72;
-constexpr int kSoftmaxRegs = 216;
+constexpr int kProducerRegs = 88;
+constexpr int kSoftmaxRegs = 208;
 static_assert(128 * (kProducerRegs + 2 * kSoftmaxRegs) <= kThreads * kLaunchRegs, "register split");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -78,9 +78,11 @@ struct Cfg {
 
 struct Shared {
   uint64_t q_full[2];
+  uint64_t q_empty[2];  // Q_i free for the next unit's load
   uint64_t s_full[2];
   uint64_t p_full[4];   // [tile][half]
   uint64_t o_done[2];
+  uint64_t o_empty[2];  // O_i read by the epilogue; the next unit may overwrite it
   uint64_t kv_full[8];
   uint64_t kv_empty[8];
   uint64_t drain;
@@ -88,12 +90,57 @@ struct Shared {
   int abort;
 };
 
+// One work unit: a pair of 128-row query tiles of one (sequence, head).
+struct Unit {
+  int b, h, hk;
+  int q_len, kv_len, q_row0, k_row0, q_start0;
+  int n_kv[2];     // K/V tiles each query tile needs (0: tile inactive)
+  bool rows;       // the unit holds at least one valid query row
+  bool bad;        // varlen offsets outside the buffers
+};
+
+// Units are numbered heaviest first: pair index descending, then (b, h); each
+// CTA takes them in snake order (see unit_of).
+__device__ __forceinline__ Unit make_unit(int u, int BH, int H, int Hkv, int n, int m,
+                                          int num_pairs, int causal, const int* cu_q,
+                                          const int* cu_k, int total_q, int total_k) {
+  Unit U;
+  const int t = num_pairs - 1 - u / BH;
+  const int bh = u % BH;
+  U.h = bh % H;
+  U.b = bh / H;
+  U.hk = U.h / (H / Hkv);
+  U.q_len = n;
+  U.kv_len = m;
+  U.q_row0 = U.b * n;
+  U.k_row0 = U.b * m;
+  U.bad = false;
+  if (cu_q != nullptr) {
+    U.q_row0 = __ldg(cu_q + U.b);
+    U.q_len = __ldg(cu_q + U.b + 1) - U.q_row0;
+    U.k_row0 = __ldg(cu_k + U.b);
+    U.kv_len = __ldg(cu_k + U.b + 1) - U.k_row0;
+    U.bad = U.q_row0 < 0 || U.q_len < 0 || U.q_row0 + U.q_len > total_q || U.k_row0 < 0 ||
+            U.kv_len < 0 || U.k_row0 + U.kv_len > total_k;
+  }
+  U.q_start0 = t * 2 * kBlockM;
+  U.rows = !U.bad && U.q_start0 < U.q_len;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int qs = U.q_start0 + i * kBlockM;
+    int keys = U.kv_len;
+    if (causal) keys = min(U.kv_len, qs + kBlockM);
+    U.n_kv[i] = (!U.rows || qs >= U.q_len || keys <= 0) ? 0 : (keys + kBlockN - 1) / kBlockN;
+  }
+  return U;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ o,
                 float* __restrict__ lse, const int* __restrict__ cu_q,
-                const int* __restrict__ cu_k, int H, int Hkv, int n, int m, int total_q,
+                const int* __restrict__ cu_k, int B, int H, int Hkv, int n, int m, int total_q,
                 int total_k, int num_pairs, float scale_log2, int causal, int lse_stride_h,
                 int lse_stride_b, int* status) {
   using C = Cfg<D>;
@@ -103,44 +150,26 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                                              ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // ---- work unit: (batch b, head h, pair t of query tiles); heaviest pairs first
-  const int bh = blockIdx.x;
-  const int h = bh % H;
-  const int b = bh / H;
-  const int t = num_pairs - 1 - (int)blockIdx.y;
-  const int hk = h / (H / Hkv);
-  int q_len = n, kv_len = m, q_row0 = b * n, k_row0 = b * m;
-  if (cu_q != nullptr) {
-    q_row0 = __ldg(cu_q + b);
-    q_len = __ldg(cu_q + b + 1) - q_row0;
-    k_row0 = __ldg(cu_k + b);
-    kv_len = __ldg(cu_k + b + 1) - k_row0;
-    if (q_row0 < 0 || q_len < 0 || q_row0 + q_len > total_q || k_row0 < 0 || kv_len < 0 ||
-        k_row0 + kv_len > total_k) {
-      if (threadIdx.x == 0) atomicExch(status, kDevInvalidArg);
-      return;  // offsets outside the buffers: skip the sequence, touch nothing
-    }
-  }
-  const int q_start0 = t * 2 * kBlockM;
-  if (q_start0 >= q_len) return;  // whole CTA idle (uniform exit before any barrier)
-  int n_kv[2];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int qs = q_start0 + i * kBlockM;
-    int keys = kv_len;
-    if (causal) keys = min(kv_len, qs + kBlockM);
-    n_kv[i] = (qs >= q_len || keys <= 0) ? 0 : (keys + kBlockN - 1) / kBlockN;
-  }
-  const int n_kv_max = max(n_kv[0], n_kv[1]);
+  const int BH = B * H;
+  const int num_units = BH * num_pairs;
+#define FA_UNIT(u) make_unit((u), BH, H, Hkv, n, m, num_pairs, causal, cu_q, cu_k, total_q, total_k)
+  // k-th unit of this CTA: waves of gridDim.x units in snake order (even waves
+  // left to right, odd waves right to left), which evens out the per-CTA sum
+  // of the heaviest-first unit sizes
+  auto unit_of = [&](int k) {
+    const int g = (int)gridDim.x;
+    return k * g + ((k & 1) ? g - 1 - (int)blockIdx.x : (int)blockIdx.x);
+  };
 
   uint8_t* sQ = smem;                        // [2][kChunks][128 rows][128 B]
   uint8_t* sKV = smem + C::kQBytes;          // [kStages][kChunks][128 rows][128 B]
 
   const uint32_t bar_q = ptx::smem_u32(&sh.q_full[0]);
+  const uint32_t bar_qe = ptx::smem_u32(&sh.q_empty[0]);
   const uint32_t bar_s = ptx::smem_u32(&sh.s_full[0]);
   const uint32_t bar_p = ptx::smem_u32(&sh.p_full[0]);
   const uint32_t bar_o = ptx::smem_u32(&sh.o_done[0]);
+  const uint32_t bar_oe = ptx::smem_u32(&sh.o_empty[0]);
   const uint32_t bar_kvf = ptx::smem_u32(&sh.kv_full[0]);
   const uint32_t bar_kve = ptx::smem_u32(&sh.kv_empty[0]);
   const uint32_t bar_drain = ptx::smem_u32(&sh.drain);
@@ -149,10 +178,12 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(bar_q + 8 * i, 1);
+      ptx::mbar_init(bar_qe + 8 * i, 1);
       ptx::mbar_init(bar_s + 8 * i, 1);
       ptx::mbar_init(bar_p + 16 * i, kBlockM);
       ptx::mbar_init(bar_p + 16 * i + 8, kBlockM);
       ptx::mbar_init(bar_o + 8 * i, 1);
+      ptx::mbar_init(bar_oe + 8 * i, kBlockM);
     }
     for (int s = 0; s < C::kStages; ++s) {
       ptx::mbar_init(bar_kvf + 8 * s, 1);
@@ -173,57 +204,67 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const uint32_t tbase = sh.tmem_base;
 
   if (warp < 4) {
-  ptx::setmaxnreg_dec<kProducerRegs>();
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    ptx::setmaxnreg_dec<kProducerRegs>();
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------- producer
       ptx::prefetch_tmap(&tmQ);
       ptx::prefetch_tmap(&tmK);
       ptx::prefetch_tmap(&tmV);
-      for (int i = 0; i < 2; ++i) {
-        if (n_kv[i] == 0) continue;
-        const uint32_t dst = ptx::smem_u32(sQ + i * C::kTileBytes);
-        ptx::mbar_arrive_expect_tx(bar_q + 8 * i, C::kTileBytes);
-#pragma unroll
-        for (int c = 0; c < C::kChunks; ++c)
-          ptx::tma_load_3d(dst + c * 16384, &tmQ, 64 * c, h, q_row0 + q_start0 + i * kBlockM,
-                           bar_q + 8 * i);
-      }
-      int issued = 0;
+      int li = 0;                 // K/V loads issued (K(j), V(j) alternate)
+      int nq[2] = {0, 0};         // Q loads issued per tile
       bool ok = true;
-      for (int j = 0; j < n_kv_max && ok; ++j) {
-        for (int which = 0; which < 2; ++which) {  // K then V
-          const int li = 2 * j + which;
-          const int slot = li % C::kStages;
-          if (!ptx::mbar_wait(bar_kve + 8 * slot, ((li / C::kStages) & 1) ^ 1, status, abort_flag)) {
-            ok = false;
-            break;
-          }
-          const uint32_t dst = ptx::smem_u32(sKV + slot * C::kTileBytes);
-          ptx::mbar_arrive_expect_tx(bar_kvf + 8 * slot, C::kTileBytes);
-          const CUtensorMap* map = which == 0 ? &tmK : &tmV;
+      for (int k = 0; k * (int)gridDim.x < num_units && ok; ++k) {
+        const int u = unit_of(k);
+        if (u >= num_units) continue;
+        const Unit U = FA_UNIT(u);
+        if (U.bad) atomicExch(status, kDevInvalidArg);  // skip the sequence, touch nothing
+        if (!U.rows) continue;
+        for (int i = 0; i < 2 && ok; ++i) {
+          if (U.n_kv[i] == 0) continue;
+          // the previous unit's last S_i MMA must be done with Q_i
+          if (!(ok = ptx::mbar_wait(bar_qe + 8 * i, (nq[i] & 1) ^ 1, status, abort_flag))) break;
+          const uint32_t dst = ptx::smem_u32(sQ + i * C::kTileBytes);
+          ptx::mbar_arrive_expect_tx(bar_q + 8 * i, C::kTileBytes);
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c)
-            ptx::tma_load_3d(dst + c * 16384, map, 64 * c, hk, k_row0 + j * kBlockN,
-                             bar_kvf + 8 * slot);
-          issued = li + 1;
+            ptx::tma_load_3d(dst + c * 16384, &tmQ, 64 * c, U.h, U.q_row0 + U.q_start0 + i * kBlockM,
+                             bar_q + 8 * i);
+          ++nq[i];
+        }
+        const int n_kv_max = max(U.n_kv[0], U.n_kv[1]);
+        for (int j = 0; j < n_kv_max && ok; ++j) {
+          for (int which = 0; which < 2; ++which) {  // K then V
+            const int slot = li % C::kStages;
+            if (!(ok = ptx::mbar_wait(bar_kve + 8 * slot, ((li / C::kStages) & 1) ^ 1, status,
+                                      abort_flag)))
+              break;
+            const uint32_t dst = ptx::smem_u32(sKV + slot * C::kTileBytes);
+            ptx::mbar_arrive_expect_tx(bar_kvf + 8 * slot, C::kTileBytes);
+            const CUtensorMap* map = which == 0 ? &tmK : &tmV;
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c)
+              ptx::tma_load_3d(dst + c * 16384, map, 64 * c, U.hk, U.k_row0 + j * kBlockN,
+                               bar_kvf + 8 * slot);
+            ++li;
+          }
         }
       }
       if (!ok) {
-        // let the last loads of every slot land before shared memory is released
-        for (int li = max(0, issued - C::kStages); li < issued; ++li)
-          ptx::mbar_wait(bar_kvf + 8 * (li % C::kStages), (li / C::kStages) & 1, nullptr);
+        // let the last load of every slot, and of every Q tile, land before
+        // shared memory is released
+        for (int l = max(0, li - C::kStages); l < li; ++l)
+          ptx::mbar_wait(bar_kvf + 8 * (l % C::kStages), (l / C::kStages) & 1, nullptr);
         for (int i = 0; i < 2; ++i)
-          if (n_kv[i] > 0) ptx::mbar_wait(bar_q + 8 * i, 0, nullptr);
+          if (nq[i] > 0) ptx::mbar_wait(bar_q + 8 * i, (nq[i] - 1) & 1, nullptr);
       }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      bool ok = true;
-      for (int i = 0; i < 2 && ok; ++i)
-        if (n_kv[i] > 0) ok = ptx::mbar_wait(bar_q + 8 * i, 0, status, abort_flag);
+    } else if (warp == 1 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
       const uint32_t q_addr[2] = {ptx::smem_u32(sQ), ptx::smem_u32(sQ + C::kTileBytes)};
+      int lc = 0;                 // K/V loads consumed
+      int nq[2] = {0, 0};         // Q tiles consumed
+      int np[2] = {0, 0};         // P tiles consumed (= S tiles issued)
+      int no[2] = {0, 0};         // units whose O_i was used
+      bool ok = true;
       auto issue_s = [&](int i, int slot) {
         const uint32_t kaddr = ptx::smem_u32(sKV + slot * C::kTileBytes);
 #pragma unroll
@@ -240,7 +281,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const uint32_t vaddr = ptx::smem_u32(sKV + slot * C::kTileBytes);
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
-          if (!ptx::mbar_wait(bar_p + 16 * i + 8 * hf, j & 1, status, abort_flag)) return false;
+          if (!ptx::mbar_wait(bar_p + 16 * i + 8 * hf, np[i] & 1, status, abort_flag)) return false;
           ptx::tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kBlockN / 32; ++kk) {
@@ -250,186 +291,225 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                         (j > 0 || k > 0) ? 1u : 0u);
           }
         }
+        ++np[i];
         return true;
       };
-      // prologue: S_i(0)
-      if (ok && n_kv_max > 0) {
-        ok = ptx::mbar_wait(bar_kvf, 0, status, abort_flag);
-        if (ok) {
+      for (int k = 0; k * (int)gridDim.x < num_units && ok; ++k) {
+        const int u = unit_of(k);
+        if (u >= num_units) continue;
+        const Unit U = FA_UNIT(u);
+        if (!U.rows) continue;
+        const int n_kv_max = max(U.n_kv[0], U.n_kv[1]);
+        if (n_kv_max == 0) continue;
+        for (int i = 0; i < 2 && ok; ++i) {
+          if (U.n_kv[i] == 0) continue;
+          ok = ptx::mbar_wait(bar_q + 8 * i, nq[i] & 1, status, abort_flag);
+          ++nq[i];
+        }
+        if (!ok) break;
+        // prologue: S_i(0)
+        {
+          const int slot = lc % C::kStages;
+          if (!(ok = ptx::mbar_wait(bar_kvf + 8 * slot, (lc / C::kStages) & 1, status, abort_flag))) break;
           ptx::tc_fence_after();
           for (int i = 0; i < 2; ++i) {
-            if (n_kv[i] == 0) continue;
-            issue_s(i, 0);
+            if (U.n_kv[i] == 0) continue;
+            issue_s(i, slot);
             ptx::tc_commit(bar_s + 8 * i);
+            if (U.n_kv[i] == 1) ptx::tc_commit(bar_qe + 8 * i);
           }
-          ptx::tc_commit(bar_kve);  // K(0) slot
+          ptx::tc_commit(bar_kve + 8 * slot);  // K(0)
         }
-      }
-      for (int j = 0; j < n_kv_max && ok; ++j) {
-        const int lv = 2 * j + 1, sv = lv % C::kStages;
-        const int lk = 2 * j + 2, sk = lk % C::kStages;
-        const bool has_next = j + 1 < n_kv_max;
-        if (!(ok = ptx::mbar_wait(bar_kvf + 8 * sv, (lv / C::kStages) & 1, status, abort_flag))) break;
-        if (j < n_kv[0]) {
-          if (!(ok = issue_pv(0, sv, j))) break;
-          if (j == n_kv[0] - 1) ptx::tc_commit(bar_o);
+        for (int j = 0; j < n_kv_max && ok; ++j) {
+          const int lv = lc + 2 * j + 1, sv = lv % C::kStages;
+          const int lk = lc + 2 * j + 2, sk = lk % C::kStages;
+          const bool has_next = j + 1 < n_kv_max;
+          if (!(ok = ptx::mbar_wait(bar_kvf + 8 * sv, (lv / C::kStages) & 1, status, abort_flag))) break;
+          // before the first P V of a unit, the previous unit's epilogue must
+          // have read O_i out of tensor memory
+          if (j < U.n_kv[0]) {
+            if (j == 0 && !(ok = ptx::mbar_wait(bar_oe, (no[0] & 1) ^ 1, status, abort_flag))) break;
+            if (!(ok = issue_pv(0, sv, j))) break;
+            if (j == U.n_kv[0] - 1) ptx::tc_commit(bar_o);
+          }
+          if (has_next) {
+            if (!(ok = ptx::mbar_wait(bar_kvf + 8 * sk, (lk / C::kStages) & 1, status, abort_flag))) break;
+            ptx::tc_fence_after();
+          }
+          if (j + 1 < U.n_kv[0]) {
+            issue_s(0, sk);
+            ptx::tc_commit(bar_s);
+            if (j + 2 == U.n_kv[0]) ptx::tc_commit(bar_qe);
+          }
+          if (j < U.n_kv[1]) {
+            if (j == 0 && !(ok = ptx::mbar_wait(bar_oe + 8, (no[1] & 1) ^ 1, status, abort_flag))) break;
+            if (!(ok = issue_pv(1, sv, j))) break;
+            if (j == U.n_kv[1] - 1) ptx::tc_commit(bar_o + 8);
+          }
+          ptx::tc_commit(bar_kve + 8 * sv);  // V(j)
+          if (j + 1 < U.n_kv[1]) {
+            issue_s(1, sk);
+            ptx::tc_commit(bar_s + 8);
+            if (j + 2 == U.n_kv[1]) ptx::tc_commit(bar_qe + 8);
+          }
+          if (has_next) ptx::tc_commit(bar_kve + 8 * sk);  // K(j+1)
         }
-        if (has_next) {
-          if (!(ok = ptx::mbar_wait(bar_kvf + 8 * sk, (lk / C::kStages) & 1, status, abort_flag))) break;
-          ptx::tc_fence_after();
-        }
-        if (j + 1 < n_kv[0]) {
-          issue_s(0, sk);
-          ptx::tc_commit(bar_s);
-        }
-        if (j < n_kv[1]) {
-          if (!(ok = issue_pv(1, sv, j))) break;
-          if (j == n_kv[1] - 1) ptx::tc_commit(bar_o + 8);
-        }
-        ptx::tc_commit(bar_kve + 8 * sv);  // V(j) slot
-        if (j + 1 < n_kv[1]) {
-          issue_s(1, sk);
-          ptx::tc_commit(bar_s + 8);
-        }
-        if (has_next) ptx::tc_commit(bar_kve + 8 * sk);  // K(j+1) slot
+        lc += 2 * n_kv_max;
+        for (int i = 0; i < 2; ++i)
+          if (U.n_kv[i] > 0) ++no[i];
       }
       // no tcgen05.mma may still run when the tensor memory is released
       ptx::tc_commit(bar_drain);
       ptx::mbar_wait(bar_drain, 0, nullptr);
     }
-  }
   } else {
     ptx::setmaxnreg_inc<kSoftmaxRegs>();
     // ------------------------------------------------------------ softmax
     const int i = (warp - 4) / 4;             // query tile of this warpgroup
     const int quarter = warp & 3;             // tensor-memory lane quarter
     const int r = quarter * 32 + lane;        // row in the tile
-    const int q_start = q_start0 + i * kBlockM;
-    const int qi = q_start + r;               // query index in the sequence
     const uint32_t lane_base = tbase + ((uint32_t)(quarter * 32) << 16);
     const uint32_t s_col = lane_base + i * kBlockN;
     const uint32_t o_col = lane_base + 256 + i * D;
-    float m_ref = -INFINITY;   // running reference (log2 units)
-    float l_run = 0.f;
+    int ns = 0;    // S tiles consumed
+    int nod = 0;   // units finished
     bool ok = true;
-    for (int j = 0; j < n_kv[i]; ++j) {
-      // warp-uniform outcome: the tcgen05.ld/st below are warp-collective
-      ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar_s + 8 * i, j & 1, status, abort_flag));
-      if (!ok) break;
-      ptx::tc_fence_after();
-      uint32_t sr[4][32];
+    for (int k = 0; k * (int)gridDim.x < num_units && ok; ++k) {
+      const int u = unit_of(k);
+      if (u >= num_units) continue;
+      const Unit U = FA_UNIT(u);
+      if (!U.rows) continue;
+      const int q_start = U.q_start0 + i * kBlockM;
+      const int qi = q_start + r;               // query index in the sequence
+      const int nkv = U.n_kv[i];
+      float m_ref = -INFINITY;   // running reference (log2 units)
+      float l_run = 0.f;
+      for (int j = 0; j < nkv; ++j) {
+        // warp-uniform outcome: the tcgen05.ld/st below are warp-collective
+        ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar_s + 8 * i, ns & 1, status, abort_flag));
+        if (!ok) break;
+        ++ns;
+        ptx::tc_fence_after();
+        uint32_t sr[4][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) ptx::tmem_ld32(s_col + c * 32, sr[c]);
-      ptx::tmem_wait_ld();
-      // mask: keys past the end, and the causal diagonal (only the last tile of a row)
-      const int k0 = j * kBlockN;
-      if (j == n_kv[i] - 1) {
-        int vis = kv_len - k0;
-        if (causal) vis = min(vis, qi - k0 + 1);
+        for (int c = 0; c < 4; ++c) ptx::tmem_ld32(s_col + c * 32, sr[c]);
+        ptx::tmem_wait_ld();
+        // mask: keys past the end, and the causal diagonal (only the last tile of a row)
+        const int k0 = j * kBlockN;
+        if (j == nkv - 1) {
+          int vis = U.kv_len - k0;
+          if (causal) vis = min(vis, qi - k0 + 1);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (c * 32 + e >= vis) sr[c][e] = __float_as_uint(-INFINITY);
+        }
+        float mx = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (c * 32 + e >= vis) sr[c][e] = __float_as_uint(-INFINITY);
-      }
-      float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int e = 0; e < 32; e += 2)
-          mx = ptx::fmax3(mx, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
-      const float m_tile = mx * scale_log2;    // scale > 0: max commutes with it
-      const bool raise = m_tile > m_ref + kRescaleThreshold || (m_ref == -INFINITY && m_tile > -INFINITY);
-      float alpha = 1.f;
-      if (raise) {
-        alpha = m_ref == -INFINITY ? 1.f : ptx::ex2(m_ref - m_tile);
-        m_ref = m_tile;
-        l_run *= alpha;
-      }
-      const float ref = m_ref == -INFINITY ? 0.f : m_ref;
-      // rescale acc first when this warp raised a reference after the first
-      // tile: no P V of this tile may run before it
-      if (__any_sync(0xffffffffu, raise && j > 0 && alpha != 1.f)) {
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t ov[32];
-          ptx::tmem_ld32(o_col + c * 32, ov);
-          ptx::tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-          ptx::tmem_st32(o_col + c * 32, ov);
+          for (int e = 0; e < 32; e += 2)
+            mx = ptx::fmax3(mx, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+        const float m_tile = mx * scale_log2;    // scale > 0: max commutes with it
+        const bool raise = m_tile > m_ref + kRescaleThreshold || (m_ref == -INFINITY && m_tile > -INFINITY);
+        float alpha = 1.f;
+        if (raise) {
+          alpha = m_ref == -INFINITY ? 1.f : ptx::ex2(m_ref - m_tile);
+          m_ref = m_tile;
+          l_run *= alpha;
         }
-      }
-      // p = 2^(s*scale*log2e - ref), two halves of 64 keys; each half is
-      // handed to the MMA warp as soon as it sits in tensor memory
-      const uint64_t sc2 = ptx::f2_bits(scale_log2, scale_log2);
-      const uint64_t nref2 = ptx::f2_bits(-ref, -ref);
-      uint64_t lsum2 = ptx::f2_bits(0.f, 0.f);
+        const float ref = m_ref == -INFINITY ? 0.f : m_ref;
+        // rescale acc first when this warp raised a reference after the first
+        // tile: no P V of this tile may run before it
+        if (__any_sync(0xffffffffu, raise && j > 0 && alpha != 1.f)) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t ov[32];
+            ptx::tmem_ld32(o_col + c * 32, ov);
+            ptx::tmem_wait_ld();
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t pr[32];
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = hf * 2 + cc;
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const uint64_t x = ptx::ffma2(
-                ptx::f2_bits(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])), sc2, nref2);
-            float x0, x1;
-            ptx::f2_split(x, x0, x1);
-            const float p0 = ptx::ex2(x0);
-            const float p1 = ptx::ex2(x1);
-            lsum2 = ptx::fadd2(lsum2, ptx::f2_bits(p0, p1));
-            pr[cc * 16 + e / 2] = ptx::pack_bf16x2(p0, p1);
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            ptx::tmem_st32(o_col + c * 32, ov);
           }
         }
-        ptx::tmem_st32(s_col + hf * 32, pr);
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar_p + 16 * i + 8 * hf);
+        // p = 2^(s*scale*log2e - ref), two halves of 64 keys; each half is
+        // handed to the MMA warp as soon as it sits in tensor memory
+        const uint64_t sc2 = ptx::f2_bits(scale_log2, scale_log2);
+        const uint64_t nref2 = ptx::f2_bits(-ref, -ref);
+        uint64_t lsum2 = ptx::f2_bits(0.f, 0.f);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t pr[32];
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int c = hf * 2 + cc;
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const uint64_t x = ptx::ffma2(
+                  ptx::f2_bits(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])), sc2, nref2);
+              float x0, x1;
+              ptx::f2_split(x, x0, x1);
+              const float p0 = ptx::ex2(x0);
+              const float p1 = ptx::ex2(x1);
+              lsum2 = ptx::fadd2(lsum2, ptx::f2_bits(p0, p1));
+              pr[cc * 16 + e / 2] = ptx::pack_bf16x2(p0, p1);
+            }
+          }
+          ptx::tmem_st32(s_col + hf * 32, pr);
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar_p + 16 * i + 8 * hf);
+        }
+        float ls0, ls1;
+        ptx::f2_split(lsum2, ls0, ls1);
+        l_run += ls0 + ls1;
       }
-      float ls0, ls1;
-      ptx::f2_split(lsum2, ls0, ls1);
-      l_run += ls0 + ls1;
-    }
+      if (!ok) break;
 
-    // ---- epilogue: O = acc / l (bf16), LSE = (ref + log2 l) ln 2
-    const bool row_valid = qi < q_len;
-    const size_t orow = (size_t)(q_row0 + qi) * H + h;
-    if (ok && n_kv[i] > 0) {
-      ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar_o + 8 * i, 0, status, abort_flag));
-      ptx::tc_fence_after();
-    }
-    if (ok) {
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      uint4* dst = reinterpret_cast<uint4*>(o + orow * D);
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t ov[32];
-        if (n_kv[i] > 0) {  // warp-uniform: every lane loads, only valid rows store
-          ptx::tmem_ld32(o_col + c * 32, ov);
-          ptx::tmem_wait_ld();
-        } else {
+      // ---- epilogue: O = acc / l (bf16), LSE = (ref + log2 l) ln 2
+      const bool row_valid = qi < U.q_len;
+      const size_t orow = (size_t)(U.q_row0 + qi) * H + U.h;
+      uint32_t ov[D / 32][32];
+      if (nkv > 0) {
+        ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar_o + 8 * i, nod & 1, status, abort_flag));
+        if (!ok) break;
+        ++nod;
+        ptx::tc_fence_after();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] = 0u;
-        }
-        if (row_valid) {
+        for (int c = 0; c < D / 32; ++c) ptx::tmem_ld32(o_col + c * 32, ov[c]);
+        ptx::tmem_wait_ld();
+        // O_i may now be overwritten by the next unit's first P V
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_oe + 8 * i);
+      } else {
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            uint4 w;
-            w.x = ptx::pack_bf16x2(__uint_as_float(ov[8 * u + 0]) * inv, __uint_as_float(ov[8 * u + 1]) * inv);
-            w.y = ptx::pack_bf16x2(__uint_as_float(ov[8 * u + 2]) * inv, __uint_as_float(ov[8 * u + 3]) * inv);
-            w.z = ptx::pack_bf16x2(__uint_as_float(ov[8 * u + 4]) * inv, __uint_as_float(ov[8 * u + 5]) * inv);
-            w.w = ptx::pack_bf16x2(__uint_as_float(ov[8 * u + 6]) * inv, __uint_as_float(ov[8 * u + 7]) * inv);
-            dst[c * 4 + u] = w;
-          }
-        }
+        for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[c][e] = 0u;
       }
-      if (row_valid && lse != nullptr)
-        lse[(size_t)b * lse_stride_b + (size_t)h * lse_stride_h + (q_row0 - (cu_q ? 0 : b * n)) + qi] =
-            l_run > 0.f ? (m_ref + __log2f(l_run)) * kLn2 : -INFINITY;
+      if (row_valid) {
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        uint4* dst = reinterpret_cast<uint4*>(o + orow * D);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            uint4 v;
+            v.x = ptx::pack_bf16x2(__uint_as_float(ov[c][8 * w + 0]) * inv, __uint_as_float(ov[c][8 * w + 1]) * inv);
+            v.y = ptx::pack_bf16x2(__uint_as_float(ov[c][8 * w + 2]) * inv, __uint_as_float(ov[c][8 * w + 3]) * inv);
+            v.z = ptx::pack_bf16x2(__uint_as_float(ov[c][8 * w + 4]) * inv, __uint_as_float(ov[c][8 * w + 5]) * inv);
+            v.w = ptx::pack_bf16x2(__uint_as_float(ov[c][8 * w + 6]) * inv, __uint_as_float(ov[c][8 * w + 7]) * inv);
+            dst[c * 4 + w] = v;
+          }
+        if (lse != nullptr)
+          lse[(size_t)U.b * lse_stride_b + (size_t)U.h * lse_stride_h +
+              (U.q_row0 - (cu_q ? 0 : U.b * n)) + qi] =
+              l_run > 0.f ? (m_ref + __log2f(l_run)) * kLn2 : -INFINITY;
+      }
     }
   }
+#undef FA_UNIT
 
   ptx::tc_fence_before();
   __syncthreads();
@@ -472,14 +552,28 @@ cudaError_t launch(const FwdParams& p, cudaStream_t stream, const char** why) {
     return e;
   }
   const int num_pairs = (p.n + 2 * kBlockM - 1) / (2 * kBlockM);
-  dim3 grid(p.B * p.H, num_pairs);
+  const long long units = (long long)p.B * p.H * num_pairs;
+  int sms = 0;
+  {
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) {
+      *why = "query SM count";
+      return e;
+    }
+  }
+  // Dense: persistent, one CTA per SM (the shared-memory footprint admits
+  // one), units in snake order.  Varlen: one CTA per unit, so the hardware
+  // block scheduler balances units whose sizes depend on lengths the host
+  // does not know (idle units exit at once).
+  const int grid = varlen ? (int)units : (int)(units < sms ? units : sms);
   // LSE layout: dense [B][H][n] ; varlen [H][Tq]
   const int lse_stride_h = varlen ? p.total_q : p.n;
   const int lse_stride_b = varlen ? 0 : p.H * p.n;
   const float scale_log2 = p.scale * kLog2e;
   fwd_bf16_kernel<D><<<grid, kThreads, C::kSmem, stream>>>(
-      tq, tk, tv, static_cast<__nv_bfloat16*>(p.o), p.lse, p.cu_q, p.cu_k, p.H, p.Hkv, p.n, p.m,
-      varlen ? p.total_q : p.B * p.n, varlen ? p.total_k : p.B * p.m, num_pairs, scale_log2,
+      tq, tk, tv, static_cast<__nv_bfloat16*>(p.o), p.lse, p.cu_q, p.cu_k, p.B, p.H, p.Hkv, p.n,
+      p.m, varlen ? p.total_q : p.B * p.n, varlen ? p.total_k : p.B * p.m, num_pairs, scale_log2,
       p.causal, lse_stride_h, lse_stride_b, p.status);
   e = cudaGetLastError();
   if (e != cudaSuccess) *why = "fwd_bf16 launch";
