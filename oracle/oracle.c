@@ -27,7 +27,10 @@
  *
  * Readings where the pages are silent (each also listed in the design notes):
  *   - LSE = M + ln(l), natural log of the summed exp of SCALED scores.
- *   - causal: key j is visible to query i iff j <= i (0-based, top-left).
+ *   - causal: key j is visible to query i iff j <= i + (m - n) (0-based;
+ *     queries are the last n of the m key positions).  For n == m this is the
+ *     pages' "the i-th query sees keys up to i"; for n > m the first n - m
+ *     queries see no key.
  *   - a row that sees no key at all: O = 0 and LSE = -inf.
  *   - grouped heads: query head h reads kv head h / (H / Hkv).
  *   - in the recurrence, a tile that is fully masked for a row while the
@@ -96,6 +99,17 @@ static void attend_one_row(const float *q, const float *k, long k_stride,
     *lse_out = M + log(l);
 }
 
+/* keys visible to query i of n, out of m: all of them, or the causal prefix
+ * j <= i + (m - n) */
+static int visible_keys(int i, int n, int m, int causal)
+{
+    if (!causal) return m;
+    long v = (long)i + 1 + ((long)m - (long)n);
+    if (v < 0) v = 0;
+    if (v > m) v = m;
+    return (int)v;
+}
+
 static int check_heads(int H, int Hkv)
 {
     return H > 0 && Hkv > 0 && H % Hkv == 0;
@@ -127,7 +141,7 @@ int oracle_attention_rows_f64(const float *q, const float *k, const float *v,
         for (int r = 0; r < R; ++r) {
             int b = rows[3 * r], h = rows[3 * r + 1], i = rows[3 * r + 2];
             int hk = h / group;
-            int m_vis = causal ? (i + 1 < m ? i + 1 : m) : m;
+            int m_vis = visible_keys(i, n, m, causal);
             const float *qi = q + (((long)b * n + i) * H + h) * d;
             const float *kb = k + ((long)b * m * Hkv + hk) * d;
             const float *vb = v + ((long)b * m * Hkv + hk) * dv;
@@ -162,7 +176,7 @@ int oracle_attention_f64(const float *q, const float *k, const float *v,
             int h = (int)((t / n) % H);
             int b = (int)(t / ((long)n * H));
             int hk = h / group;
-            int m_vis = causal ? (i + 1 < m ? i + 1 : m) : m;
+            int m_vis = visible_keys(i, n, m, causal);
             const float *qi = q + (((long)b * n + i) * H + h) * d;
             const float *kb = k + ((long)b * m * Hkv + hk) * d;
             const float *vb = v + ((long)b * m * Hkv + hk) * dv;
@@ -179,7 +193,7 @@ int oracle_attention_f64(const float *q, const float *k, const float *v,
  * Variable-length (packed) attention.  Sequence s owns query tokens
  * [cu_q[s], cu_q[s+1]) and key tokens [cu_k[s], cu_k[s+1]).
  * q [Tq][H][d], k [Tk][Hkv][d], v [Tk][Hkv][dv]; o [Tq][H][dv]; lse [H][Tq].
- * Causal: local key j visible to local query i iff j <= i.
+ * Causal: local key j visible to local query i iff j <= i + (m_s - n_s).
  */
 int oracle_varlen_f64(const float *q, const float *k, const float *v,
                       const int *cu_q, const int *cu_k, int num_seqs, int H,
@@ -205,7 +219,7 @@ int oracle_varlen_f64(const float *q, const float *k, const float *v,
             while (cu_q[s + 1] <= tok) ++s; /* sequence owning this token */
             int i = tok - cu_q[s];
             int m = cu_k[s + 1] - cu_k[s];
-            int m_vis = causal ? (i + 1 < m ? i + 1 : m) : m;
+            int m_vis = visible_keys(i, cu_q[s + 1] - cu_q[s], m, causal);
             int hk = h / group;
             const float *qi = q + ((long)tok * H + h) * d;
             const float *kb = k + ((long)cu_k[s] * Hkv + hk) * d;
@@ -459,7 +473,7 @@ int oracle_online_recurrence_f64(const float *q, const float *k, const float *v,
                 double m_blk = -INFINITY;
                 for (int c = 0; c < cols; ++c) {
                     int j = j0 + c;
-                    if (causal && j > i) {
+                    if (causal && (long)j > (long)i + ((long)m - (long)n)) {
                         s[c] = -INFINITY;
                         continue;
                     }

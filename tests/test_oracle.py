@@ -33,11 +33,20 @@ def _sdpa_f64(q, k, v, scale, causal):
     qt = torch.from_numpy(q.astype(np.float64)).permute(0, 2, 1, 3)
     kt = torch.from_numpy(k.astype(np.float64)).permute(0, 2, 1, 3).repeat_interleave(g, dim=1)
     vt = torch.from_numpy(v.astype(np.float64)).permute(0, 2, 1, 3).repeat_interleave(g, dim=1)
-    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=scale, is_causal=causal)
+    n_, m_ = qt.shape[-2], kt.shape[-2]
+    # causal, bottom-right aligned: key j visible to query i iff j <= i + (m - n)
+    mask = torch.ones(n_, m_, dtype=torch.bool).tril(diagonal=m_ - n_) if causal else None
+    if mask is not None and not mask.any(dim=-1).all():
+        # rows that see no key: the library routine returns NaN there, the
+        # reading is O = 0, LSE = -inf; evaluate the others only
+        o = torch.zeros(qt.shape[:-1] + (vt.shape[-1],), dtype=torch.float64)
+        keep = mask.any(dim=-1)
+        o[..., keep, :] = torch.nn.functional.scaled_dot_product_attention(
+            qt[..., keep, :], kt, vt, attn_mask=mask[keep], scale=scale)
+    else:
+        o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=scale)
     s = torch.einsum("bhid,bhjd->bhij", qt, kt) * scale
     if causal:
-        n_, m_ = s.shape[-2:]
-        mask = torch.ones(n_, m_, dtype=torch.bool).tril()
         s = s.masked_fill(~mask, float("-inf"))
     lse = torch.logsumexp(s, dim=-1)
     return o.permute(0, 2, 1, 3).numpy(), lse.numpy()
@@ -76,6 +85,28 @@ def test_q_zero_causal_is_prefix_mean():
             want = v[0, : i + 1, h].astype(np.float64).mean(axis=0)
             np.testing.assert_allclose(o[0, i, h], want, rtol=0, atol=1e-14)
             assert abs(lse[0, h, i] - math.log(i + 1)) < 1e-14
+
+
+@pytest.mark.parametrize("n,m", [(4, 9), (9, 4), (1, 7)])
+def test_q_zero_causal_unequal_lengths_bottom_right(n, m):
+    """Causal with n != m, read bottom-right: the n queries are the last n of
+    the m key positions, so row i sees keys 0..i+(m-n); with Q = 0 it is the
+    mean of those V rows and LSE = ln(count).  Rows that see none (n > m) get
+    O = 0 and LSE = -inf."""
+    H, d, dv = 2, 4, 3
+    q = np.zeros((1, n, H, d), np.float32)
+    k = _rand(41, 1, m, H, d)
+    v = _rand(42, 1, m, H, dv)
+    o, lse = oracle.attention(q, k, v, 1.0, causal=True)
+    for h in range(H):
+        for i in range(n):
+            cnt = min(m, max(0, i + 1 + m - n))
+            if cnt == 0:
+                assert np.all(o[0, i, h] == 0) and np.isneginf(lse[0, h, i])
+                continue
+            want = v[0, :cnt, h].astype(np.float64).mean(axis=0)
+            np.testing.assert_allclose(o[0, i, h], want, rtol=0, atol=1e-14)
+            assert abs(lse[0, h, i] - math.log(cnt)) < 1e-14
 
 
 def test_one_dominant_score_selects_its_value_row():
@@ -150,7 +181,8 @@ def test_key_shift_invariance():
 # ----------------------------------------------------------------------------
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("shape", [(1, 1, 1, 1, 1, 4, 4), (2, 4, 2, 9, 9, 8, 8),
-                                   (1, 6, 3, 5, 12, 16, 8), (3, 2, 2, 16, 16, 4, 7)])
+                                   (1, 6, 3, 5, 12, 16, 8), (3, 2, 2, 16, 16, 4, 7),
+                                   (1, 2, 1, 12, 5, 8, 8)])
 def test_brute_force_vs_library_sdpa(shape, causal):
     B, H, Hkv, n, m, d, dv = shape
     q, k, v = _rand(20, B, n, H, d, scale=2), _rand(21, B, m, Hkv, d, scale=2), _rand(22, B, m, Hkv, dv)
@@ -196,6 +228,17 @@ def test_recurrence_any_tile_equals_definition(kv_block, causal):
     o_def, l_def = oracle.attention(q[None, :, None], k[None, :, None], v[None, :, None], 0.3, causal)
     np.testing.assert_allclose(o_rec, o_def[0, :, 0], rtol=0, atol=1e-12)
     np.testing.assert_allclose(l_rec, l_def[0, 0], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("n,m", [(40, 130), (130, 40)])
+def test_recurrence_unequal_causal_equals_definition(n, m):
+    q, k, v = _rand(36, n, 8, scale=2), _rand(37, m, 8, scale=2), _rand(38, m, 8)
+    o_rec, l_rec = oracle.online_recurrence(q, k, v, 0.4, True, q_block=16, kv_block=32)
+    o_def, l_def = oracle.attention(q[None, :, None], k[None, :, None], v[None, :, None], 0.4, True)
+    np.testing.assert_allclose(o_rec, o_def[0, :, 0], rtol=0, atol=1e-12)
+    assert np.array_equal(np.isneginf(l_rec), np.isneginf(l_def[0, 0]))
+    fin = ~np.isneginf(l_rec)
+    np.testing.assert_allclose(l_rec[fin], l_def[0, 0][fin], rtol=0, atol=1e-12)
 
 
 def test_recurrence_guard_fully_masked_first_tiles():
