@@ -30,8 +30,10 @@
  *   - bf16 values are IEEE bfloat16 bit patterns (uint16 storage); outputs O
  *     are rounded to bf16 with round-to-nearest-even; LSE is float32.
  *   - A query row that sees no key gets O = 0 and LSE = -inf.
- *   - Causal: key j is visible to query i iff j <= i (0-based, top-left);
- *     it requires n == m (per sequence for varlen).
+ *   - Causal: key j is visible to query i iff j <= i + (m - n) (0-based):
+ *     the n queries are the last n of the m key positions.  For n == m this
+ *     is "query i sees the keys up to i"; for n > m the first n - m queries
+ *     see no key (O = 0, LSE = -inf).  Varlen applies it per sequence.
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
@@ -46,7 +48,7 @@ typedef enum {
     FA_OK = 0,
     FA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, H % Hkv != 0, misaligned pointer */
     FA_ERR_UNSUPPORTED = 2,   /* valid but not implemented: d/dv/page_size outside the supported set,
-                                 causal with n != m, no sm_103a device */
+                                 no sm_103a device */
     FA_ERR_WORKSPACE = 3,     /* workspace pointer null or smaller than the size query returns */
     FA_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed; fa_last_error() has the text */
     FA_ERR_TIMEOUT = 5,       /* device status: a pipeline wait exceeded its limit */
@@ -66,7 +68,7 @@ typedef enum {
  *   lse  fp32 [B][H][n]          written (may be NULL: not written)
  *   scale  multiplies Q K^T; must be positive and finite (pass 1/sqrt(d)
  *          for the usual attention)
- *   causal 0 or 1 (1 requires n == m)
+ *   causal 0 or 1
  * Supported: d == dv, d in {64, 128}; pointers 16-byte aligned; n, m >= 0.
  * Computes S = Q K^T and P V on the tcgen05 tensor cores (bf16 operands,
  * fp32 accumulation in tensor memory); P is rounded to bf16 before P V.
@@ -103,9 +105,7 @@ fa_status fa_forward_f32(const float* q, const float* k, const float* v, float* 
  *        device status word)
  *   max_seqlen_q, max_seqlen_k  upper bounds of the per-sequence lengths
  *        (sizes the launch grid; a larger value only launches idle blocks)
- * Supported as fa_forward; causal needs equal q and k lengths per sequence
- * (the call cannot check this on the host; unequal lengths give the
- * top-left-aligned mask).
+ * Supported as fa_forward; causal uses each sequence's own q and k lengths.
  */
 fa_status fa_forward_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
                             const int* cu_seqlens_q, const int* cu_seqlens_k, int num_seqs,

@@ -70,6 +70,12 @@ def _check_rows(case, o, lse, rows):
     (1, 2, 1, 129, 129, 64, False),
     (1, 2, 2, 384, 384, 128, True),
     (3, 2, 1, 640, 100, 64, False),
+    # causal with n != m: bottom-right (queries are the last n key positions)
+    (1, 2, 1, 100, 300, 128, True),
+    (2, 4, 2, 300, 100, 64, True),
+    (1, 2, 2, 129, 700, 128, True),
+    (1, 8, 2, 64, 1000, 128, True),
+    (1, 2, 1, 1, 513, 64, True),
 ])
 def test_small_shapes(shape):
     B, H, Hkv, n, m, d, causal = shape
@@ -175,3 +181,25 @@ def test_varlen_offsets_outside_buffers_are_rejected_on_device():
     fb.fa_forward_varlen(q, k, v, o, None, dev_i32(cu_bad), dev_i32(cu_bad), 2, 30, 30, 999, 999,
                          2, 2, 64, 64, case.scale, 1)
     assert fb.fa_get_device_status() == fb.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_varlen_causal_unequal_q_and_k_lengths(d):
+    """Chunked-prefill shape: each sequence's queries are its last q_len key
+    positions (bottom-right causal), with q_len < k_len, = k_len and > k_len."""
+    q_lens = [50, 128, 200, 1, 300]
+    k_lens = [400, 128, 120, 77, 1000]
+    H, Hkv = 4, 2
+    cu_q = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(k_lens)]).astype(np.int32)
+    g = I.rng(45, d)
+    q = I.Tensor.from_f32(I.normal_f32(g, (int(cu_q[-1]), H, d)), "bf16")
+    k = I.Tensor.from_f32(I.normal_f32(g, (int(cu_k[-1]), Hkv, d)), "bf16")
+    v = I.Tensor.from_f32(I.normal_f32(g, (int(cu_k[-1]), Hkv, d)), "bf16")
+    scale = I.fp32_scale(d)
+    o, lse = fb.forward_varlen(dev(q), dev(k), dev(v), dev_i32(cu_q), dev_i32(cu_k), max(q_lens),
+                               max(k_lens), scale, True)
+    o_ref, lse_ref = oracle.varlen(q.values, k.values, v.values, cu_q, cu_k, scale, True)
+    assert_close(host(o), o_ref, BF16_MAX_ABS, BF16_MEAN_ABS, what=f"varlen q!=k d={d}")
+    assert_lse_close(host(lse), lse_ref, what=f"varlen q!=k d={d}")
+    assert fb.fa_get_device_status() == 0

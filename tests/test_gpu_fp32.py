@@ -37,6 +37,8 @@ def test_c1_single_head_256(hot):
     (2, 2, 2, 1, 1, 64, 128, False),
     (1, 2, 1, 97, 97, 128, 64, True),
     (1, 1, 1, 5, 333, 64, 64, False),
+    (1, 2, 1, 40, 130, 64, 64, True),
+    (2, 2, 2, 130, 40, 128, 128, True),
 ])
 def test_fp32_shapes(shape):
     B, H, Hkv, n, m, d, dv, causal = shape

@@ -67,8 +67,6 @@ fa_status check_dense(const void* q, const void* k, const void* v, const void* o
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u))
     return fail(FA_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned (lse 4-byte)", fn);
-  if (causal && n != m)
-    return fail(FA_ERR_UNSUPPORTED, "%s: causal needs n == m (got n=%d m=%d)", fn, n, m);
   return FA_OK;
 }
 

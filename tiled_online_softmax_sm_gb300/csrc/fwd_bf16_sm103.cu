@@ -31,7 +31,8 @@
 // LSE = (ref + log2 l) ln 2 are exact in any case.  While a row has seen only
 // masked keys its reference is 0, so exp(-inf - -inf) never occurs ("S12
 // FlashAttention", 实现).  Whole K/V tiles above the causal diagonal are never
-// loaded or multiplied ("手搓 Attention" §6).
+// loaded or multiplied ("手搓 Attention" §6).  Causal is aligned bottom-right:
+// query i of n sees keys j <= i + (m - n) (top-left when n == m).
 //
 // Every mbarrier wait is bounded; on a timeout the CTA records it in the
 // device status word, stops issuing work, lets copies in flight land and
@@ -128,8 +129,8 @@ __device__ __forceinline__ Unit make_unit(int u, int BH, int H, int Hkv, int n, 
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const int qs = U.q_start0 + i * kBlockM;
-    int keys = U.kv_len;
-    if (causal) keys = min(U.kv_len, qs + kBlockM);
+    int keys = U.kv_len;   // causal: the tile's last row sees keys < qs + 128 + (m - n)
+    if (causal) keys = min(U.kv_len, qs + kBlockM + (U.kv_len - U.q_len));
     U.n_kv[i] = (!U.rows || qs >= U.q_len || keys <= 0) ? 0 : (keys + kBlockN - 1) / kBlockN;
   }
   return U;
@@ -394,11 +395,13 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
         for (int c = 0; c < 4; ++c) ptx::tmem_ld32(s_col + c * 32, sr[c]);
         ptx::tmem_wait_ld();
-        // mask: keys past the end, and the causal diagonal (only the last tile of a row)
+        // mask keys past the end and, causal, keys j > qi + (m - n): only tiles
+        // that reach past the end or past the tile's first row's diagonal
         const int k0 = j * kBlockN;
-        if (j == nkv - 1) {
+        const int diag = q_start + (U.kv_len - U.q_len);   // last key row q_start sees
+        if (k0 + kBlockN > U.kv_len || (causal && k0 + kBlockN - 1 > diag)) {
           int vis = U.kv_len - k0;
-          if (causal) vis = min(vis, qi - k0 + 1);
+          if (causal) vis = min(vis, qi + (U.kv_len - U.q_len) - k0 + 1);
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll

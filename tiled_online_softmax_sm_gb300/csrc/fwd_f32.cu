@@ -98,7 +98,8 @@ fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
   float l_run = 0.f;
 
   int kv_end = m;
-  if (causal) kv_end = min(m, q0 + kRowsPerCta);
+  const int off = m - n;  // causal, bottom-right: query i sees keys j <= i + off
+  if (causal) kv_end = min(m, q0 + kRowsPerCta + off);
   const size_t k_row_stride = (size_t)Hkv * D;
   const size_t v_row_stride = (size_t)Hkv * DV;
   const float* kbase = k + ((size_t)b * m * Hkv + hk) * D;
@@ -120,7 +121,7 @@ fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
     __syncthreads();
 
     int vis = cols;                 // visible keys of this row in the tile: [0, vis)
-    if (causal) vis = min(vis, i - j0 + 1);
+    if (causal) vis = min(vis, i + off - j0 + 1);
     if (!row_valid) vis = 0;
 
     float s_hi[kTileN], s_lo[kTileN];
