@@ -54,11 +54,13 @@ def _load():
             lib.oracle_attention_f64.argtypes = [P, P, P, I, I, I, I, I, I, I, D, I, P, P]
             lib.oracle_varlen_f64.argtypes = [P, P, P, P, P, I, I, I, I, I, D, I, P, P]
             lib.oracle_paged_decode_f64.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, D, P, P]
+            lib.oracle_paged_prefill_f64.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, D, I, P, P]
             lib.oracle_decode_partials_f64.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, D, P, P, P]
             lib.oracle_split_combine_f64.argtypes = [P, P, P, I, I, I, I, P, P]
             lib.oracle_online_recurrence_f64.argtypes = [P, P, P, I, I, I, I, D, I, I, I, P, P, P]
             for f in ("oracle_attention_rows_f64", "oracle_attention_f64", "oracle_varlen_f64",
-                      "oracle_paged_decode_f64", "oracle_decode_partials_f64",
+                      "oracle_paged_decode_f64", "oracle_paged_prefill_f64",
+                      "oracle_decode_partials_f64",
                       "oracle_split_combine_f64", "oracle_online_recurrence_f64",
                       "oracle_num_threads"):
                 getattr(lib, f).restype = ctypes.c_int
@@ -165,6 +167,27 @@ def paged_decode(q, k_cache, v_cache, block_table, seq_lens, scale):
                                          Hkv, d, dv, page, P, bt.shape[1], float(scale),
                                          _ptr(o), _ptr(lse))
     _check(rc, "oracle.paged_decode")
+    return o, lse
+
+
+def paged_prefill(q, cu_q, k_cache, v_cache, block_table, seq_lens, scale, causal=True):
+    """Several query tokens per sequence against its paged keys.
+
+    q [Tq,H,d] packed by cu_q [S+1]; caches [P,Hkv,page,d]; block_table
+    [S,max_blocks]; seq_lens [S] keys per sequence -> (o [Tq,H,dv], lse [H,Tq]).
+    Causal: the queries are the last n_s of the seq_lens[s] positions.
+    """
+    q, kc, vc = _f32(q), _f32(k_cache), _f32(v_cache)
+    cu, bt, sl = _i32(cu_q), _i32(block_table), _i32(seq_lens)
+    Tq, H, d = q.shape
+    P, Hkv, page, dv = vc.shape
+    S = cu.shape[0] - 1
+    o = np.empty((Tq, H, dv), np.float64)
+    lse = np.empty((H, Tq), np.float64)
+    rc = _load().oracle_paged_prefill_f64(_ptr(q), _ptr(cu), _ptr(kc), _ptr(vc), _ptr(bt), _ptr(sl),
+                                          S, H, Hkv, d, dv, page, P, bt.shape[1], float(scale),
+                                          int(bool(causal)), _ptr(o), _ptr(lse))
+    _check(rc, "oracle.paged_prefill")
     return o, lse
 
 

@@ -297,6 +297,80 @@ int oracle_paged_decode_f64(const float *q, const float *k_cache, const float *v
 }
 
 /*
+ * Paged prefill: several new query tokens per sequence against the sequence's
+ * paged keys ([p2] 它还解锁了什么: the tiles the recurrence walks need not be
+ * contiguous, each may come through the block table).  Sequence s owns query
+ * tokens [cu_q[s], cu_q[s+1]) (n_s of them) and seq_lens[s] keys gathered page
+ * by page as in oracle_paged_decode_f64.  Causal: the queries are the last n_s
+ * of the seq_lens[s] positions, so query i sees keys j <= i + (seq_lens[s] - n_s).
+ * q [Tq][H][d]; o [Tq][H][dv]; lse [H][Tq].
+ * Returns 0, -1 on invalid arguments, -2 on a block-table id out of range.
+ */
+int oracle_paged_prefill_f64(const float *q, const int *cu_q, const float *k_cache,
+                             const float *v_cache, const int *block_table, const int *seq_lens,
+                             int num_seqs, int H, int Hkv, int d, int dv, int page_size,
+                             int num_pages, int max_blocks, double scale, int causal,
+                             double *o, double *lse)
+{
+    if (!check_heads(H, Hkv) || num_seqs < 0 || d <= 0 || dv <= 0 || page_size <= 0)
+        return -1;
+    for (int s = 0; s < num_seqs; ++s) {
+        if (cu_q[s + 1] < cu_q[s]) return -1;
+        if (seq_lens[s] < 0 || seq_lens[s] > max_blocks * page_size) return -1;
+        int pages = (seq_lens[s] + page_size - 1) / page_size;
+        for (int p = 0; p < pages; ++p) {
+            int phys = block_table[(long)s * max_blocks + p];
+            if (phys < 0 || phys >= num_pages) return -2;
+        }
+    }
+    const int group = H / Hkv;
+    const int Tq = num_seqs > 0 ? cu_q[num_seqs] : 0;
+    const long total = (long)num_seqs * Hkv;
+    int ok = 0;
+#pragma omp parallel reduction(| : ok)
+    {
+        int cap = max_blocks * page_size > 0 ? max_blocks * page_size : 1;
+        float *kg = (float *)malloc(sizeof(float) * (size_t)cap * d);
+        float *vg = (float *)malloc(sizeof(float) * (size_t)cap * dv);
+        double *scores = (double *)malloc(sizeof(double) * (size_t)cap);
+        if (!kg || !vg || !scores) ok |= 1;
+#pragma omp for schedule(dynamic, 1)
+        for (long t = 0; t < total; ++t) {
+            if (!kg || !vg || !scores) continue;
+            int s = (int)(t / Hkv), hk = (int)(t % Hkv);
+            /* gather this sequence's keys and values for kv head hk */
+            int count = 0;
+            for (int logical = 0; logical < max_blocks; ++logical) {
+                int nvalid = seq_lens[s] - logical * page_size;
+                if (nvalid > page_size) nvalid = page_size;
+                if (nvalid <= 0) break;
+                int phys = block_table[(long)s * max_blocks + logical];
+                const float *kp = k_cache + (((long)phys * Hkv + hk) * page_size) * d;
+                const float *vp = v_cache + (((long)phys * Hkv + hk) * page_size) * dv;
+                for (int r = 0; r < nvalid; ++r) {
+                    memcpy(kg + (long)count * d, kp + (long)r * d, sizeof(float) * d);
+                    memcpy(vg + (long)count * dv, vp + (long)r * dv, sizeof(float) * dv);
+                    ++count;
+                }
+            }
+            const int n = cu_q[s + 1] - cu_q[s];
+            for (int h = hk * group; h < (hk + 1) * group; ++h)
+                for (int i = 0; i < n; ++i) {
+                    int tok = cu_q[s] + i;
+                    attend_one_row(q + ((long)tok * H + h) * d, kg, d, vg, dv,
+                                   visible_keys(i, n, count, causal), d, dv, scale,
+                                   o + ((long)tok * H + h) * dv, lse + (long)h * Tq + tok, NULL,
+                                   scores);
+                }
+        }
+        free(kg);
+        free(vg);
+        free(scores);
+    }
+    return ok ? -1 : 0;
+}
+
+/*
  * Flash-decoding partials ([p2] 它还解锁了什么, 练习 1): the keys of each
  * sequence are cut into num_splits page-aligned ranges; split x covers logical
  * pages [ceil(x*P/X), ceil((x+1)*P/X)) of the sequence's P pages.  For each

@@ -284,6 +284,40 @@ def test_paged_decode_matches_dense_library():
         np.testing.assert_allclose(lse[s], l_ref[0, :, 0], rtol=0, atol=1e-12)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_paged_prefill_matches_dense_library(causal):
+    """Several new tokens per sequence against the sequence's paged keys equal
+    the library routine on the gathered keys with the bottom-right mask."""
+    lens = [1, 4, 5, 17, 30]
+    q_lens = [1, 3, 5, 7, 40]          # the last sequence has more queries than keys
+    case = I.decode_case(12, num_seqs=5, H=4, Hkv=2, d=16, dv=16, page_size=4, lens=lens,
+                         max_blocks=9)
+    cu = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    q = _rand(13, int(cu[-1]), 4, 16)
+    o, lse = oracle.paged_prefill(q, cu, case.k_cache.values, case.v_cache.values,
+                                  case.block_table, case.seq_lens, case.scale, causal)
+    assert np.isfinite(o).all()   # poisoned slots never read
+    for s, (kk, vv) in enumerate(_dense_gather(case)):
+        a, b = cu[s], cu[s + 1]
+        o_ref, l_ref = _sdpa_f64(q[None, a:b], kk[None], vv[None], case.scale, causal)
+        np.testing.assert_allclose(o[a:b], o_ref[0], rtol=0, atol=1e-12)
+        assert np.array_equal(np.isneginf(lse[:, a:b]), np.isneginf(l_ref[0]))
+        fin = ~np.isneginf(l_ref[0])
+        np.testing.assert_allclose(lse[:, a:b][fin], l_ref[0][fin], rtol=0, atol=1e-12)
+
+
+def test_paged_prefill_single_token_is_decode():
+    case = I.decode_case(14, num_seqs=3, H=4, Hkv=1, d=8, page_size=4, lens=[3, 9, 16],
+                         max_blocks=4)
+    cu = np.arange(4, dtype=np.int32)
+    a = oracle.paged_prefill(case.q.values, cu, case.k_cache.values, case.v_cache.values,
+                             case.block_table, case.seq_lens, case.scale, True)
+    b = oracle.paged_decode(case.q.values, case.k_cache.values, case.v_cache.values,
+                            case.block_table, case.seq_lens, case.scale)
+    np.testing.assert_allclose(a[0], b[0], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(a[1].T, b[1], rtol=0, atol=1e-14)
+
+
 def test_paged_decode_rejects_bad_block_ids():
     case = I.decode_case(8, num_seqs=2, H=2, Hkv=1, d=8, page_size=4, lens=[5, 3], max_blocks=2)
     bt = case.block_table.copy()
