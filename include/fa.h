@@ -113,6 +113,41 @@ fa_status fa_forward_varlen(const void* q, const void* k, const void* v, void* o
                             int H, int Hkv, int d, int dv, float scale, int causal, void* stream);
 
 /*
+ * fa_paged_prefill — bf16 attention for several new query tokens per
+ * sequence against that sequence's paged keys (chunked prefill).
+ * Passage: "S12 FlashAttention", 它还解锁了什么 (the tiles the recurrence walks
+ * need not be contiguous: each can be fetched through a block table) and 实现
+ * (logical page p holds min(page_size, seq_len - p*page_size) valid tokens).
+ *
+ *   q            bf16 [total_q][H][d], sequence s owns rows
+ *                [cu_seqlens_q[s], cu_seqlens_q[s+1])
+ *   k_cache      bf16 [num_pages][Hkv][page_size][d]
+ *   v_cache      bf16 [num_pages][Hkv][page_size][dv]
+ *   block_table  int32 [num_seqs][max_blocks_per_seq]: logical -> physical page
+ *   seq_lens     int32 [num_seqs]: keys of sequence s (its cached context and
+ *                its new tokens), 0 <= seq_lens[s] <= max_blocks_per_seq*page_size
+ *   cu_seqlens_q int32 [num_seqs + 1], non-decreasing from 0 to total_q
+ *   o            bf16 [total_q][H][dv] written
+ *   lse          fp32 [H][total_q]     written (may be NULL)
+ *   max_seqlen_q upper bound of the per-sequence query counts
+ *   causal       0 or 1: with 1 the n_s queries of sequence s are the last n_s
+ *                of its seq_lens[s] positions (query i sees keys j <= i +
+ *                seq_lens[s] - n_s)
+ * All of K/V is read through TMA a page at a time on the tcgen05 path of
+ * fa_forward.  Cache contents past seq_lens[s] in the last page are never
+ * used, NaN included.  Page ids are range-checked on the device (an id
+ * outside [0, num_pages) reads page 0 and sets FA_ERR_BAD_BLOCK_TABLE);
+ * sequences whose query offsets fall outside total_q, or whose seq_lens
+ * exceed the table, are skipped and set FA_ERR_INVALID_ARG.
+ * Supported: d == dv in {64, 128}, page_size == 16.
+ */
+fa_status fa_paged_prefill(const void* q, const void* k_cache, const void* v_cache,
+                           const int* block_table, const int* seq_lens, const int* cu_seqlens_q,
+                           void* o, float* lse, int num_seqs, int total_q, int max_seqlen_q,
+                           int H, int Hkv, int d, int dv, int page_size, int num_pages,
+                           int max_blocks_per_seq, float scale, int causal, void* stream);
+
+/*
  * fa_paged_decode_workspace_size — bytes of workspace fa_paged_decode needs:
  * the per-split partial triples (m, l: fp32 [num_seqs][H][num_splits] each;
  * o: fp32 [num_seqs][H][num_splits][dv]), each array 256-byte aligned.

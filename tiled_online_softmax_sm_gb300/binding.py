@@ -28,7 +28,8 @@ FA_ERR_CUDA = 4
 FA_ERR_TIMEOUT = 5
 FA_ERR_BAD_BLOCK_TABLE = 6
 
-EXPORTED = ("fa_forward", "fa_forward_f32", "fa_forward_varlen", "fa_paged_decode_workspace_size",
+EXPORTED = ("fa_forward", "fa_forward_f32", "fa_forward_varlen", "fa_paged_prefill",
+            "fa_paged_decode_workspace_size",
             "fa_paged_decode", "fa_paged_decode_noalloc", "fa_split_combine", "fa_last_error",
             "fa_get_device_status")
 FA_NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -58,6 +59,7 @@ def load(path: str = LIB_PATH):
         lib.fa_forward.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, I, P]
         lib.fa_forward_f32.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, I, P]
         lib.fa_forward_varlen.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, I, P]
+        lib.fa_paged_prefill.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, F, I, P]
         lib.fa_paged_decode_workspace_size.argtypes = [I, I, I, I]
         lib.fa_paged_decode_workspace_size.restype = Z
         lib.fa_paged_decode.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, P, Z, P]
@@ -66,7 +68,8 @@ def load(path: str = LIB_PATH):
         lib.fa_last_error.argtypes = []
         lib.fa_last_error.restype = ctypes.c_char_p
         lib.fa_get_device_status.argtypes = [P, ctypes.POINTER(I)]
-        for name in ("fa_forward", "fa_forward_f32", "fa_forward_varlen", "fa_paged_decode",
+        for name in ("fa_forward", "fa_forward_f32", "fa_forward_varlen", "fa_paged_prefill",
+                     "fa_paged_decode",
                      "fa_paged_decode_noalloc", "fa_split_combine", "fa_get_device_status"):
             getattr(lib, name).restype = I
         _lib = lib
@@ -114,6 +117,15 @@ def fa_forward_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, num_seqs, tot
                                     _p(cu_seqlens_k), num_seqs, total_q, total_k, max_seqlen_q,
                                     max_seqlen_k, H, Hkv, d, dv, float(scale), int(causal),
                                     _stream(stream)))
+
+
+def fa_paged_prefill(q, k_cache, v_cache, block_table, seq_lens, cu_seqlens_q, o, lse, num_seqs,
+                     total_q, max_seqlen_q, H, Hkv, d, dv, page_size, num_pages,
+                     max_blocks_per_seq, scale, causal, stream=None):
+    _check(load().fa_paged_prefill(_p(q), _p(k_cache), _p(v_cache), _p(block_table), _p(seq_lens),
+                                   _p(cu_seqlens_q), _p(o), _p(lse), num_seqs, total_q,
+                                   max_seqlen_q, H, Hkv, d, dv, page_size, num_pages,
+                                   max_blocks_per_seq, float(scale), int(causal), _stream(stream)))
 
 
 def fa_paged_decode_workspace_size(num_seqs, H, dv, num_splits) -> int:
@@ -191,6 +203,21 @@ def forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen
     lse = torch.empty((H, Tq), dtype=torch.float32, device=q.device)
     fa_forward_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, S, Tq, Tk, max_seqlen_q,
                       max_seqlen_k, H, Hkv, d, dv, scale, causal, stream)
+    return o, lse
+
+
+def paged_prefill(q, k_cache, v_cache, block_table, seq_lens, cu_seqlens_q, max_seqlen_q, scale,
+                  causal=True, stream=None):
+    """q [Tq,H,d] packed by cu_seqlens_q; caches [P,Hkv,page,d] -> (o [Tq,H,dv], lse [H,Tq])."""
+    import torch
+    Tq, H, d = q.shape
+    P, Hkv, page, dv = v_cache.shape
+    S = cu_seqlens_q.shape[0] - 1
+    o = torch.empty((Tq, H, dv), dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((H, Tq), dtype=torch.float32, device=q.device)
+    fa_paged_prefill(q, k_cache, v_cache, block_table, seq_lens, cu_seqlens_q, o, lse, S, Tq,
+                     max_seqlen_q, H, Hkv, d, dv, page, P, block_table.shape[1], scale, causal,
+                     stream)
     return o, lse
 
 

@@ -166,6 +166,49 @@ fa_status fa_forward_varlen(const void* q, const void* k, const void* v, void* o
   return FA_OK;
 }
 
+fa_status fa_paged_prefill(const void* q, const void* k_cache, const void* v_cache,
+                           const int* block_table, const int* seq_lens, const int* cu_seqlens_q,
+                           void* o, float* lse, int num_seqs, int total_q, int max_seqlen_q,
+                           int H, int Hkv, int d, int dv, int page_size, int num_pages,
+                           int max_blocks_per_seq, float scale, int causal, void* stream) {
+  const char* fn = "fa_paged_prefill";
+  if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || num_pages < 0 || max_blocks_per_seq < 0)
+    return fail(FA_ERR_INVALID_ARG, "%s: negative size", fn);
+  if (H <= 0 || Hkv <= 0 || H % Hkv != 0)
+    return fail(FA_ERR_INVALID_ARG, "%s: H=%d Hkv=%d (need H %% Hkv == 0)", fn, H, Hkv);
+  if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARG, "%s: causal=%d", fn, causal);
+  if (!(scale > 0.f) || scale == INFINITY)
+    return fail(FA_ERR_INVALID_ARG, "%s: scale must be positive and finite", fn);
+  if (!(d == dv && (d == 64 || d == 128)))
+    return fail(FA_ERR_UNSUPPORTED, "%s: d=%d dv=%d (supported: d == dv in {64, 128})", fn, d, dv);
+  if (page_size != 16) return fail(FA_ERR_UNSUPPORTED, "%s: page_size=%d (supported: 16)", fn, page_size);
+  if (num_seqs == 0 || total_q == 0 || max_seqlen_q == 0) return FA_OK;
+  if (q == nullptr || o == nullptr || k_cache == nullptr || v_cache == nullptr ||
+      block_table == nullptr || seq_lens == nullptr || cu_seqlens_q == nullptr)
+    return fail(FA_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (num_pages == 0 || max_blocks_per_seq == 0)
+    return fail(FA_ERR_INVALID_ARG, "%s: empty page pool or block table", fn);
+  if ((long long)num_pages * Hkv * 16 > 0x7fffffffLL)
+    return fail(FA_ERR_UNSUPPORTED, "%s: page pool too large", fn);
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(block_table) & 3u) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u) || (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u))
+    return fail(FA_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
+  int* sp = nullptr;
+  fa_status st = status_ptr(&sp);
+  if (st != FA_OK) return st;
+  fa::FwdParams p{q, k_cache, v_cache, o, lse, cu_seqlens_q, nullptr, num_seqs, H, Hkv,
+                  max_seqlen_q, 0, d, dv, total_q, 0, scale, causal, sp};
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_pages = num_pages;
+  const char* why = nullptr;
+  cudaError_t e = fa::launch_fwd_bf16(p, static_cast<cudaStream_t>(stream), &why);
+  if (e != cudaSuccess) return cuda_fail(e, why ? why : "fa_paged_prefill launch");
+  return FA_OK;
+}
+
 static size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 size_t fa_paged_decode_workspace_size(int num_seqs, int H, int dv, int num_splits) {

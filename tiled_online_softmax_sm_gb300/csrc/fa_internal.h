@@ -26,6 +26,12 @@ struct FwdParams {
   float scale;
   int causal;
   int* status;         // device status word
+  // paged prefill (block_table != nullptr): k, v are caches [pages][Hkv][16][d],
+  // seq_lens[b] keys per sequence, q packed by cu_q as for varlen
+  const int* block_table = nullptr;
+  const int* seq_lens = nullptr;
+  int max_blocks = 0;
+  int num_pages = 0;
 };
 
 struct DecodeParams {

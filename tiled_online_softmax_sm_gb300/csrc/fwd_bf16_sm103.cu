@@ -87,6 +87,7 @@ struct Shared {
   uint64_t kv_full[8];
   uint64_t kv_empty[8];
   uint64_t drain;
+  uint64_t fix;         // paged: a V tile that reaches past the end, before zeroing
   uint32_t tmem_base;
   int abort;
 };
@@ -104,7 +105,8 @@ struct Unit {
 // CTA takes them in snake order (see unit_of).
 __device__ __forceinline__ Unit make_unit(int u, int BH, int H, int Hkv, int n, int m,
                                           int num_pairs, int causal, const int* cu_q,
-                                          const int* cu_k, int total_q, int total_k) {
+                                          const int* cu_k, int total_q, int total_k,
+                                          const int* seq_lens, int max_blocks) {
   Unit U;
   const int t = num_pairs - 1 - u / BH;
   const int bh = u % BH;
@@ -116,7 +118,14 @@ __device__ __forceinline__ Unit make_unit(int u, int BH, int H, int Hkv, int n, 
   U.q_row0 = U.b * n;
   U.k_row0 = U.b * m;
   U.bad = false;
-  if (cu_q != nullptr) {
+  if (seq_lens != nullptr) {  // paged: keys through the block table
+    U.q_row0 = __ldg(cu_q + U.b);
+    U.q_len = __ldg(cu_q + U.b + 1) - U.q_row0;
+    U.k_row0 = 0;
+    U.kv_len = __ldg(seq_lens + U.b);
+    U.bad = U.q_row0 < 0 || U.q_len < 0 || U.q_row0 + U.q_len > total_q || U.kv_len < 0 ||
+            U.kv_len > max_blocks * 16;
+  } else if (cu_q != nullptr) {
     U.q_row0 = __ldg(cu_q + U.b);
     U.q_len = __ldg(cu_q + U.b + 1) - U.q_row0;
     U.k_row0 = __ldg(cu_k + U.b);
@@ -136,14 +145,18 @@ __device__ __forceinline__ Unit make_unit(int u, int BH, int H, int Hkv, int n, 
   return U;
 }
 
-template <int D>
+// PAGED: K and V come from page caches [pages][Hkv][16][d] through the block
+// table (2-D tensor maps, one 16-row box per page), seq_lens gives each
+// sequence's key count; otherwise K/V are dense or packed rows (3-D maps).
+template <int D, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ o,
                 float* __restrict__ lse, const int* __restrict__ cu_q,
                 const int* __restrict__ cu_k, int B, int H, int Hkv, int n, int m, int total_q,
                 int total_k, int num_pairs, float scale_log2, int causal, int lse_stride_h,
-                int lse_stride_b, int* status) {
+                int lse_stride_b, const int* __restrict__ block_table,
+                const int* __restrict__ seq_lens, int max_blocks, int num_pages, int* status) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ Shared sh;
@@ -153,7 +166,9 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const int lane = threadIdx.x & 31;
   const int BH = B * H;
   const int num_units = BH * num_pairs;
-#define FA_UNIT(u) make_unit((u), BH, H, Hkv, n, m, num_pairs, causal, cu_q, cu_k, total_q, total_k)
+#define FA_UNIT(u)                                                                            \
+  make_unit((u), BH, H, Hkv, n, m, num_pairs, causal, cu_q, cu_k, total_q, total_k,              \
+            PAGED ? seq_lens : nullptr, max_blocks)
   // k-th unit of this CTA: waves of gridDim.x units in snake order (even waves
   // left to right, odd waves right to left), which evens out the per-CTA sum
   // of the heaviest-first unit sizes
@@ -174,6 +189,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const uint32_t bar_kvf = ptx::smem_u32(&sh.kv_full[0]);
   const uint32_t bar_kve = ptx::smem_u32(&sh.kv_empty[0]);
   const uint32_t bar_drain = ptx::smem_u32(&sh.drain);
+  const uint32_t bar_fix = ptx::smem_u32(&sh.fix);
   volatile int* abort_flag = &sh.abort;
 
   if (threadIdx.x == 0) {
@@ -191,6 +207,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       ptx::mbar_init(bar_kve + 8 * s, 1);
     }
     ptx::mbar_init(bar_drain, 1);
+    ptx::mbar_init(bar_fix, 1);
     sh.abort = 0;
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
@@ -206,57 +223,112 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 
   if (warp < 4) {
     ptx::setmaxnreg_dec<kProducerRegs>();
-    if (warp == 0 && lane == 0) {
+    if (warp == 0) {
       // ---------------------------------------------------------- producer
-      ptx::prefetch_tmap(&tmQ);
-      ptx::prefetch_tmap(&tmK);
-      ptx::prefetch_tmap(&tmV);
+      // The whole warp walks the schedule; lane 0 issues the copies, and in
+      // paged mode all lanes zero the V rows past a sequence's end.
+      if (lane == 0) {
+        ptx::prefetch_tmap(&tmQ);
+        ptx::prefetch_tmap(&tmK);
+        ptx::prefetch_tmap(&tmV);
+      }
       int li = 0;                 // K/V loads issued (K(j), V(j) alternate)
       int nq[2] = {0, 0};         // Q loads issued per tile
+      int nfix = 0;               // V tiles zero-fixed (paged)
+      bool fix_pending = false;
       bool ok = true;
       for (int k = 0; k * (int)gridDim.x < num_units && ok; ++k) {
         const int u = unit_of(k);
         if (u >= num_units) continue;
         const Unit U = FA_UNIT(u);
-        if (U.bad) atomicExch(status, kDevInvalidArg);  // skip the sequence, touch nothing
+        if (U.bad && lane == 0) atomicExch(status, kDevInvalidArg);  // skip it, touch nothing
         if (!U.rows) continue;
         for (int i = 0; i < 2 && ok; ++i) {
           if (U.n_kv[i] == 0) continue;
           // the previous unit's last S_i MMA must be done with Q_i
           if (!(ok = ptx::mbar_wait(bar_qe + 8 * i, (nq[i] & 1) ^ 1, status, abort_flag))) break;
-          const uint32_t dst = ptx::smem_u32(sQ + i * C::kTileBytes);
-          ptx::mbar_arrive_expect_tx(bar_q + 8 * i, C::kTileBytes);
+          if (lane == 0) {
+            const uint32_t dst = ptx::smem_u32(sQ + i * C::kTileBytes);
+            ptx::mbar_arrive_expect_tx(bar_q + 8 * i, C::kTileBytes);
 #pragma unroll
-          for (int c = 0; c < C::kChunks; ++c)
-            ptx::tma_load_3d(dst + c * 16384, &tmQ, 64 * c, U.h, U.q_row0 + U.q_start0 + i * kBlockM,
-                             bar_q + 8 * i);
+            for (int c = 0; c < C::kChunks; ++c)
+              ptx::tma_load_3d(dst + c * 16384, &tmQ, 64 * c, U.h,
+                               U.q_row0 + U.q_start0 + i * kBlockM, bar_q + 8 * i);
+          }
           ++nq[i];
         }
         const int n_kv_max = max(U.n_kv[0], U.n_kv[1]);
         for (int j = 0; j < n_kv_max && ok; ++j) {
-          for (int which = 0; which < 2; ++which) {  // K then V
+          for (int which = 0; which < 2 && ok; ++which) {  // K then V
             const int slot = li % C::kStages;
             if (!(ok = ptx::mbar_wait(bar_kve + 8 * slot, ((li / C::kStages) & 1) ^ 1, status,
                                       abort_flag)))
               break;
-            const uint32_t dst = ptx::smem_u32(sKV + slot * C::kTileBytes);
-            ptx::mbar_arrive_expect_tx(bar_kvf + 8 * slot, C::kTileBytes);
+            __syncwarp();
+            uint8_t* tile = sKV + slot * C::kTileBytes;
+            const uint32_t dst = ptx::smem_u32(tile);
             const CUtensorMap* map = which == 0 ? &tmK : &tmV;
+            if constexpr (PAGED) {
+              const int rows_valid = min(kBlockN, U.kv_len - j * kBlockN);
+              const int npages = (rows_valid + 15) / 16;
+              // a V tile reaching past the end lands on the fix barrier first
+              const bool fix = which == 1 && rows_valid < kBlockN;
+              const uint32_t bar = fix ? bar_fix : bar_kvf + 8 * slot;
+              if (lane == 0) {
+                ptx::mbar_arrive_expect_tx(bar, npages * 16 * D * 2);
+                const int* bt_row = block_table + (size_t)U.b * max_blocks + j * (kBlockN / 16);
+                for (int pg = 0; pg < npages; ++pg) {
+                  int id = __ldg(bt_row + pg);
+                  if (id < 0 || id >= num_pages) {
+                    atomicExch(status, kDevBadBlockTable);
+                    id = 0;
+                  }
+                  const int row = (id * Hkv + U.hk) * 16;
 #pragma unroll
-            for (int c = 0; c < C::kChunks; ++c)
-              ptx::tma_load_3d(dst + c * 16384, map, 64 * c, U.hk, U.k_row0 + j * kBlockN,
-                               bar_kvf + 8 * slot);
+                  for (int c = 0; c < C::kChunks; ++c)
+                    ptx::tma_load_2d(dst + c * 16384 + pg * 2048, map, 64 * c, row, bar);
+                }
+              }
+              if (fix) {
+                fix_pending = true;
+                if (!(ok = ptx::mbar_wait(bar_fix, nfix & 1, status, abort_flag))) break;
+                fix_pending = false;
+                ++nfix;
+                // rows past the end: whatever the cache holds there (NaN
+                // included) must not reach P V, where 0 * NaN = NaN
+                const int zero_rows = kBlockN - rows_valid;
+                for (int idx = lane; idx < zero_rows * 8 * C::kChunks; idx += 32) {
+                  const int c = idx / (zero_rows * 8);
+                  const int rem = idx % (zero_rows * 8);
+                  const int row = rows_valid + rem / 8;
+                  *reinterpret_cast<uint4*>(tile + c * 16384 + row * 128 + (rem % 8) * 16) =
+                      make_uint4(0u, 0u, 0u, 0u);
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar_kvf + 8 * slot);
+              }
+            } else {
+              if (lane == 0) {
+                ptx::mbar_arrive_expect_tx(bar_kvf + 8 * slot, C::kTileBytes);
+#pragma unroll
+                for (int c = 0; c < C::kChunks; ++c)
+                  ptx::tma_load_3d(dst + c * 16384, map, 64 * c, U.hk, U.k_row0 + j * kBlockN,
+                                   bar_kvf + 8 * slot);
+              }
+            }
             ++li;
           }
         }
       }
-      if (!ok) {
+      if (!ok && lane == 0) {
         // let the last load of every slot, and of every Q tile, land before
         // shared memory is released
         for (int l = max(0, li - C::kStages); l < li; ++l)
           ptx::mbar_wait(bar_kvf + 8 * (l % C::kStages), (l / C::kStages) & 1, nullptr);
         for (int i = 0; i < 2; ++i)
           if (nq[i] > 0) ptx::mbar_wait(bar_q + 8 * i, (nq[i] - 1) & 1, nullptr);
+        if (fix_pending) ptx::mbar_wait(bar_fix, nfix & 1, nullptr);
       }
     } else if (warp == 1 && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
@@ -522,7 +594,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   }
 }
 
-template <int D>
+template <int D, bool PAGED>
 cudaError_t launch(const FwdParams& p, cudaStream_t stream, const char** why) {
   using C = Cfg<D>;
   const bool varlen = p.cu_q != nullptr;
@@ -539,7 +611,17 @@ cudaError_t launch(const FwdParams& p, cudaStream_t stream, const char** why) {
       return cudaErrorInvalidValue;
     }
   }
-  {
+  if (PAGED) {
+    // 2-D views (dim, page row) of the caches; one box = one page of one kv head
+    const uint64_t dims[2] = {(uint64_t)D, (uint64_t)p.num_pages * p.Hkv * 16};
+    const uint64_t strides[1] = {(uint64_t)D * 2};
+    const uint32_t pbox[2] = {64, 16};
+    if (!make_tmap_bf16(&tk, p.k, 2, dims, strides, pbox) ||
+        !make_tmap_bf16(&tv, p.v, 2, dims, strides, pbox)) {
+      *why = "tensor map for the k/v caches";
+      return cudaErrorInvalidValue;
+    }
+  } else {
     const uint64_t dims[3] = {(uint64_t)D, (uint64_t)p.Hkv, k_rows > 0 ? k_rows : 1};
     const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)p.Hkv * D * 2};
     if (!make_tmap_bf16(&tk, p.m > 0 ? p.k : p.q, 3, dims, strides, box) ||
@@ -548,7 +630,7 @@ cudaError_t launch(const FwdParams& p, cudaStream_t stream, const char** why) {
       return cudaErrorInvalidValue;
     }
   }
-  cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D>,
+  cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D, PAGED>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) {
     *why = "cudaFuncSetAttribute(fwd_bf16)";
@@ -566,18 +648,19 @@ cudaError_t launch(const FwdParams& p, cudaStream_t stream, const char** why) {
     }
   }
   // Dense: persistent, one CTA per SM (the shared-memory footprint admits
-  // one), units in snake order.  Varlen: one CTA per unit, so the hardware
-  // block scheduler balances units whose sizes depend on lengths the host
-  // does not know (idle units exit at once).
+  // one), units in snake order.  Varlen and paged: one CTA per unit, so the
+  // hardware block scheduler balances units whose sizes depend on lengths
+  // the host does not know (idle units exit at once).
   const int grid = varlen ? (int)units : (int)(units < sms ? units : sms);
-  // LSE layout: dense [B][H][n] ; varlen [H][Tq]
+  // LSE layout: dense [B][H][n] ; varlen and paged [H][Tq]
   const int lse_stride_h = varlen ? p.total_q : p.n;
   const int lse_stride_b = varlen ? 0 : p.H * p.n;
   const float scale_log2 = p.scale * kLog2e;
-  fwd_bf16_kernel<D><<<grid, kThreads, C::kSmem, stream>>>(
+  fwd_bf16_kernel<D, PAGED><<<grid, kThreads, C::kSmem, stream>>>(
       tq, tk, tv, static_cast<__nv_bfloat16*>(p.o), p.lse, p.cu_q, p.cu_k, p.B, p.H, p.Hkv, p.n,
       p.m, varlen ? p.total_q : p.B * p.n, varlen ? p.total_k : p.B * p.m, num_pairs, scale_log2,
-      p.causal, lse_stride_h, lse_stride_b, p.status);
+      p.causal, lse_stride_h, lse_stride_b, p.block_table, p.seq_lens, p.max_blocks, p.num_pages,
+      p.status);
   e = cudaGetLastError();
   if (e != cudaSuccess) *why = "fwd_bf16 launch";
   return e;
@@ -586,8 +669,9 @@ cudaError_t launch(const FwdParams& p, cudaStream_t stream, const char** why) {
 }  // namespace
 
 cudaError_t launch_fwd_bf16(const FwdParams& p, cudaStream_t stream, const char** why) {
-  if (p.d == 128 && p.dv == 128) return launch<128>(p, stream, why);
-  if (p.d == 64 && p.dv == 64) return launch<64>(p, stream, why);
+  const bool paged = p.block_table != nullptr;
+  if (p.d == 128 && p.dv == 128) return paged ? launch<128, true>(p, stream, why) : launch<128, false>(p, stream, why);
+  if (p.d == 64 && p.dv == 64) return paged ? launch<64, true>(p, stream, why) : launch<64, false>(p, stream, why);
   *why = "fwd_bf16: unsupported head dim";
   return cudaErrorInvalidValue;
 }
