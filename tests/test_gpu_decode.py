@@ -153,3 +153,47 @@ def _c4_ref():
     if "ref" not in _cache:
         _cache["ref"] = _oracle(_c4())
     return _cache["ref"]
+
+
+def test_decode_step_replays_from_a_cuda_graph():
+    """A decode step (split partials + merge) captured once in a CUDA graph and
+    replayed gives the eager result bit for bit, also after the inputs change
+    in place (pointers fixed, contents new)."""
+    case = I.decode_case(12, num_seqs=8, H=32, Hkv=8, d=128,
+                         lens=[17, 300, 1024, 5, 2048, 129, 700, 64], max_blocks=128)
+    q, kc, vc = dev(case.q), dev(case.k_cache), dev(case.v_cache)
+    bt, sl = dev_i32(case.block_table), dev_i32(case.seq_lens)
+    S, X = 8, 8
+    need = fb.fa_paged_decode_workspace_size(S, case.H, case.dv, X)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    o = torch.empty((S, case.H, case.dv), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((S, case.H), dtype=torch.float32, device="cuda")
+
+    def step(stream=None):
+        fb.fa_paged_decode(q, kc, vc, bt, sl, o, lse, S, case.H, case.Hkv, case.d, case.dv,
+                           case.page_size, case.num_pages, case.max_blocks, X, case.scale, ws,
+                           need, stream)
+
+    step()                       # eager: also does the one-time set-up
+    torch.cuda.synchronize()
+    o_eager, l_eager = o.clone(), lse.clone()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            step(s)
+    o.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o.view(torch.int16), o_eager.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), l_eager.view(torch.int32))
+    # new query contents, same pointers: the replay follows them
+    q.copy_(torch.flip(q, dims=[0]))
+    step()
+    torch.cuda.synchronize()
+    o_eager2 = o.clone()
+    o.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o.view(torch.int16), o_eager2.view(torch.int16))
+    assert not torch.equal(o_eager2.view(torch.int16), o_eager.view(torch.int16))
