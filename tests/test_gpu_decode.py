@@ -6,6 +6,8 @@ laid out contiguously behind an identity table must give identical bits.
 Unused pool pages and the tail slots of each last page hold NaN, so a stray
 read shows up as NaN in O.
 """
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -197,3 +199,21 @@ def test_decode_step_replays_from_a_cuda_graph():
     torch.cuda.synchronize()
     assert torch.equal(o.view(torch.int16), o_eager2.view(torch.int16))
     assert not torch.equal(o_eager2.view(torch.int16), o_eager.view(torch.int16))
+
+
+def test_wait_timeout_sets_status_and_context_stays_usable(monkeypatch):
+    """Failure detection without a fault: with the test hook set, each decode
+    warp never requests its first page, its bounded wait runs out (~1 s), the
+    kernel records FA_ERR_TIMEOUT and returns.  The next call, hook unset,
+    runs normally on the same context."""
+    case = I.decode_case(13, num_seqs=1, H=8, Hkv=2, d=128, lens=[100], max_blocks=8)
+    monkeypatch.setenv("FA_TEST_FORCE_WAIT_TIMEOUT", "1")
+    t0 = time.time()
+    _gpu_decode(case, 1)
+    assert fb.fa_get_device_status() == fb.FA_ERR_TIMEOUT
+    assert time.time() - t0 < 30
+    monkeypatch.delenv("FA_TEST_FORCE_WAIT_TIMEOUT")
+    o, lse = _gpu_decode(case, 2)
+    assert fb.fa_get_device_status() == 0
+    o_ref, lse_ref = _oracle(case)
+    assert_close(host(o), o_ref, BF16_MAX_ABS, BF16_MEAN_ABS)

@@ -29,6 +29,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include "fa_internal.h"
 #include "ptx.cuh"
@@ -77,7 +78,7 @@ decode_partials_kernel(const __grid_constant__ CUtensorMap tmK,
                        const int* __restrict__ seq_lens, int num_seqs, int H, int Hkv,
                        int num_pages, int max_blocks, int X, float scale_log2,
                        float* __restrict__ part_m, float* __restrict__ part_l,
-                       float* __restrict__ part_o, int* status) {
+                       float* __restrict__ part_o, int* status, int skip_first_copy) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -104,6 +105,9 @@ decode_partials_kernel(const __grid_constant__ CUtensorMap tmK,
     ptx::prefetch_tmap(&tmK);
     ptx::prefetch_tmap(&tmV);
     for (int it = 0; it < kStages && pb + it < pe; ++it) {
+      // test hook: with skip_first_copy the first page is never requested, so
+      // its wait runs out and the timeout path (status, drain, return) runs
+      if (skip_first_copy && it == 0) continue;
       bool bad;
       int id = page_id(bt_row, pb + it, num_pages, bad);
       if (bad) atomicExch(status, kDevBadBlockTable);
@@ -328,6 +332,15 @@ split_combine_kernel(const float* __restrict__ part_m, const float* __restrict__
   if (lane == 0 && lse != nullptr) lse[t] = l > 0.f ? M + logf(l) : -INFINITY;
 }
 
+// Failure-detection test hook: FA_TEST_FORCE_WAIT_TIMEOUT=1 in the
+// environment makes every decode warp skip its first page copy, so its
+// bounded wait expires (after ~1 s), FA_ERR_TIMEOUT is recorded and the warp
+// returns without writing its partials.  Unset in normal use.
+int skip_first_copy_for_tests() {
+  const char* v = getenv("FA_TEST_FORCE_WAIT_TIMEOUT");
+  return (v != nullptr && v[0] == '1') ? 1 : 0;
+}
+
 }  // namespace
 
 cudaError_t launch_decode_partials(const DecodeParams& p, cudaStream_t stream) {
@@ -348,7 +361,7 @@ cudaError_t launch_decode_partials(const DecodeParams& p, cudaStream_t stream) {
   decode_partials_kernel<<<grid, kWarps * 32, kSmemBytes, stream>>>(
       tmK, tmV, static_cast<const __nv_bfloat16*>(p.q), p.block_table, p.seq_lens, p.num_seqs,
       p.H, p.Hkv, p.num_pages, p.max_blocks, p.num_splits, p.scale * kLog2e, p.part_m, p.part_l,
-      p.part_o, p.status);
+      p.part_o, p.status, skip_first_copy_for_tests());
   return cudaGetLastError();
 }
 
