@@ -338,20 +338,26 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       int np[2] = {0, 0};         // P tiles consumed (= S tiles issued)
       int no[2] = {0, 0};         // units whose O_i was used
       bool ok = true;
+      // Descriptors are built once; an MMA step only adds the byte offset of
+      // its operand (in 16-byte units) to the start-address field (bits 0-13,
+      // which cannot carry: shared addresses are below 256 KB).  This keeps
+      // the single issuing thread to a few instructions per MMA.
+      const uint64_t qdesc[2] = {ptx::smem_desc_sw128(q_addr[0], 16, 1024),
+                                 ptx::smem_desc_sw128(q_addr[1], 16, 1024)};
+      const uint64_t kdesc0 = ptx::smem_desc_sw128(ptx::smem_u32(sKV), 16, 1024);
+      const uint64_t vdesc0 = ptx::smem_desc_sw128(ptx::smem_u32(sKV), 16384, 1024);
       auto issue_s = [&](int i, int slot) {
-        const uint32_t kaddr = ptx::smem_u32(sKV + slot * C::kTileBytes);
+        const uint64_t kd = kdesc0 + (uint64_t)(slot * (C::kTileBytes >> 4));
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          const uint64_t ad = ptx::smem_desc_sw128(q_addr[i] + off, 16, 1024);
-          const uint64_t bd = ptx::smem_desc_sw128(kaddr + off, 16, 1024);
-          ptx::mma_ss(tbase + i * kBlockN, ad, bd, C::kIdescS, k > 0);
+          const uint32_t off = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
+          ptx::mma_ss(tbase + i * kBlockN, qdesc[i] + off, kd + off, C::kIdescS, k > 0);
         }
       };
       // O_i += P_i V(j) in two halves of 64 keys, each issued once the softmax
       // warps have stored that half of P; false if a wait failed
       auto issue_pv = [&](int i, int slot, int j) -> bool {
-        const uint32_t vaddr = ptx::smem_u32(sKV + slot * C::kTileBytes);
+        const uint64_t vd = vdesc0 + (uint64_t)(slot * (C::kTileBytes >> 4));
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           if (!ptx::mbar_wait(bar_p + 16 * i + 8 * hf, np[i] & 1, status, abort_flag)) return false;
@@ -359,9 +365,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
           for (int kk = 0; kk < kBlockN / 32; ++kk) {
             const int k = hf * (kBlockN / 32) + kk;
-            const uint64_t bd = ptx::smem_desc_sw128(vaddr + k * 2048, 16384, 1024);
-            ptx::mma_ts(tbase + 256 + i * D, tbase + i * kBlockN + k * 8, bd, C::kIdescO,
-                        (j > 0 || k > 0) ? 1u : 0u);
+            ptx::mma_ts(tbase + 256 + i * D, tbase + i * kBlockN + k * 8, vd + (uint64_t)(k * 128),
+                        C::kIdescO, (j > 0 || k > 0) ? 1u : 0u);
           }
         }
         ++np[i];
@@ -480,12 +485,20 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             for (int e = 0; e < 32; ++e)
               if (c * 32 + e >= vis) sr[c][e] = __float_as_uint(-INFINITY);
         }
-        float mx = -INFINITY;
+        // row max as 8 independent chains (a single chain would be 64
+        // dependent instructions on the critical path), then a small tree
+        float mxs[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) mxs[a] = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; e += 2)
-            mx = ptx::fmax3(mx, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+          for (int e = 0; e < 32; e += 2) {
+            const int a = (c * 16 + e / 2) & 7;
+            mxs[a] = ptx::fmax3(mxs[a], __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+          }
+        const float mx = ptx::fmax3(ptx::fmax3(mxs[0], mxs[1], mxs[2]),
+                                    ptx::fmax3(mxs[3], mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7]));
         const float m_tile = mx * scale_log2;    // scale > 0: max commutes with it
         const bool raise = m_tile > m_ref + kRescaleThreshold || (m_ref == -INFINITY && m_tile > -INFINITY);
         float alpha = 1.f;
@@ -512,7 +525,9 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // handed to the MMA warp as soon as it sits in tensor memory
         const uint64_t sc2 = ptx::f2_bits(scale_log2, scale_log2);
         const uint64_t nref2 = ptx::f2_bits(-ref, -ref);
-        uint64_t lsum2 = ptx::f2_bits(0.f, 0.f);
+        uint64_t lsum2[4];   // four independent packed partial sums
+#pragma unroll
+        for (int a = 0; a < 4; ++a) lsum2[a] = ptx::f2_bits(0.f, 0.f);
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t pr[32];
@@ -527,7 +542,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
               ptx::f2_split(x, x0, x1);
               const float p0 = ptx::ex2(x0);
               const float p1 = ptx::ex2(x1);
-              lsum2 = ptx::fadd2(lsum2, ptx::f2_bits(p0, p1));
+              lsum2[(e / 2) & 3] = ptx::fadd2(lsum2[(e / 2) & 3], ptx::f2_bits(p0, p1));
               pr[cc * 16 + e / 2] = ptx::pack_bf16x2(p0, p1);
             }
           }
@@ -537,7 +552,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           ptx::mbar_arrive(bar_p + 16 * i + 8 * hf);
         }
         float ls0, ls1;
-        ptx::f2_split(lsum2, ls0, ls1);
+        ptx::f2_split(ptx::fadd2(ptx::fadd2(lsum2[0], lsum2[1]), ptx::fadd2(lsum2[2], lsum2[3])), ls0,
+                      ls1);
         l_run += ls0 + ls1;
       }
       if (!ok) break;
