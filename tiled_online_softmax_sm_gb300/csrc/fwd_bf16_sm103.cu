@@ -415,6 +415,10 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             if (!(ok = issue_pv(0, sv, j))) break;
             if (j == U.n_kv[0] - 1) ptx::tc_commit(bar_o);
           }
+          // release K(j) (last read by S_i(j), issued in the previous
+          // iteration) here, behind a burst of queued MMAs rather than in the
+          // gap after S_1(j); K(0) was released in the prologue
+          if (j > 0) ptx::tc_commit(bar_kve + 8 * ((lc + 2 * j) % C::kStages));
           if (has_next) {
             if (!(ok = ptx::mbar_wait(bar_kvf + 8 * sk, (lk / C::kStages) & 1, status, abort_flag))) break;
             ptx::tc_fence_after();
@@ -435,7 +439,6 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             ptx::tc_commit(bar_s + 8);
             if (j + 2 == U.n_kv[1]) ptx::tc_commit(bar_qe + 8);
           }
-          if (has_next) ptx::tc_commit(bar_kve + 8 * sk);  // K(j+1)
         }
         lc += 2 * n_kv_max;
         for (int i = 0; i < 2; ++i)
