@@ -78,6 +78,24 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
                      float scale, int causal, void* stream);
 
 /*
+ * fa_forward_fp8 — attention forward with e4m3 (FP8) operands and per-tensor
+ * descale factors: the values are q[i] * q_descale, k[j] * k_descale,
+ * v[j] * v_descale.  Same shapes, layouts and semantics as fa_forward; o is
+ * bf16, lse fp32 (of the descaled scores).  The pages name FP8 only as a
+ * later FlashAttention feature ("S12 FlashAttention", 生产实践); the
+ * recurrence is unchanged: S = Q K^T and P V run on the tcgen05 tensor cores
+ * in kind::f8f6f4 with fp32 accumulation, and P is rounded to e4m3 (it lies
+ * in [0, 256] under the lazy rescale, inside e4m3's range) before P V.
+ *   q, k, v   e4m3 bytes [B][n][H][d], [B][m][Hkv][d], [B][m][Hkv][dv]
+ *   descales  positive finite fp32
+ * Supported: d == dv == 128.
+ */
+fa_status fa_forward_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int H, int Hkv, int n, int m, int d, int dv, float scale,
+                         float q_descale, float k_descale, float v_descale, int causal,
+                         void* stream);
+
+/*
  * fa_forward_f32 — fp32 attention forward, dense batch; same shapes, layouts
  * and semantics as fa_forward with every tensor in float32.  Arithmetic is
  * IEEE fp32 on the CUDA cores (no TF32); each score is carried as a

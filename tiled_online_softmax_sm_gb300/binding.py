@@ -28,7 +28,7 @@ FA_ERR_CUDA = 4
 FA_ERR_TIMEOUT = 5
 FA_ERR_BAD_BLOCK_TABLE = 6
 
-EXPORTED = ("fa_forward", "fa_forward_f32", "fa_forward_varlen", "fa_paged_prefill",
+EXPORTED = ("fa_forward", "fa_forward_fp8", "fa_forward_f32", "fa_forward_varlen", "fa_paged_prefill",
             "fa_paged_decode_workspace_size",
             "fa_paged_decode", "fa_paged_decode_noalloc", "fa_split_combine", "fa_last_error",
             "fa_get_device_status")
@@ -58,6 +58,7 @@ def load(path: str = LIB_PATH):
         P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.fa_forward.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, I, P]
         lib.fa_forward_f32.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, I, P]
+        lib.fa_forward_fp8.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, F, F, F, I, P]
         lib.fa_forward_varlen.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, I, P]
         lib.fa_paged_prefill.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, F, I, P]
         lib.fa_paged_decode_workspace_size.argtypes = [I, I, I, I]
@@ -68,7 +69,8 @@ def load(path: str = LIB_PATH):
         lib.fa_last_error.argtypes = []
         lib.fa_last_error.restype = ctypes.c_char_p
         lib.fa_get_device_status.argtypes = [P, ctypes.POINTER(I)]
-        for name in ("fa_forward", "fa_forward_f32", "fa_forward_varlen", "fa_paged_prefill",
+        for name in ("fa_forward", "fa_forward_fp8", "fa_forward_f32", "fa_forward_varlen",
+                     "fa_paged_prefill",
                      "fa_paged_decode",
                      "fa_paged_decode_noalloc", "fa_split_combine", "fa_get_device_status"):
             getattr(lib, name).restype = I
@@ -104,6 +106,13 @@ def _check(rc: int):
 def fa_forward(q, k, v, o, lse, B, H, Hkv, n, m, d, dv, scale, causal, stream=None):
     _check(load().fa_forward(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, Hkv, n, m, d, dv,
                              float(scale), int(causal), _stream(stream)))
+
+
+def fa_forward_fp8(q, k, v, o, lse, B, H, Hkv, n, m, d, dv, scale, q_descale, k_descale,
+                   v_descale, causal, stream=None):
+    _check(load().fa_forward_fp8(_p(q), _p(k), _p(v), _p(o), _p(lse), B, H, Hkv, n, m, d, dv,
+                                 float(scale), float(q_descale), float(k_descale),
+                                 float(v_descale), int(causal), _stream(stream)))
 
 
 def fa_forward_f32(q, k, v, o, lse, B, H, Hkv, n, m, d, dv, scale, causal, stream=None):
@@ -179,6 +188,18 @@ def forward(q, k, v, scale, causal=False, stream=None):
     o = torch.empty((B, n, H, dv), dtype=torch.bfloat16, device=q.device)
     lse = torch.empty((B, H, n), dtype=torch.float32, device=q.device)
     fa_forward(q, k, v, o, lse, B, H, Hkv, n, m, d, dv, scale, causal, stream)
+    return o, lse
+
+
+def forward_fp8(q, k, v, scale, q_descale, k_descale, v_descale, causal=False, stream=None):
+    """e4m3 q [B,n,H,d], k/v [B,m,Hkv,d] (uint8 or float8 tensors) -> (o bf16, lse fp32)."""
+    import torch
+    B, n, H, d = q.shape
+    _, m, Hkv, dv = v.shape
+    o = torch.empty((B, n, H, dv), dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((B, H, n), dtype=torch.float32, device=q.device)
+    fa_forward_fp8(q, k, v, o, lse, B, H, Hkv, n, m, d, dv, scale, q_descale, k_descale, v_descale,
+                   causal, stream)
     return o, lse
 
 

@@ -120,6 +120,34 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
   return FA_OK;
 }
 
+fa_status fa_forward_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                         int H, int Hkv, int n, int m, int d, int dv, float scale,
+                         float q_descale, float k_descale, float v_descale, int causal,
+                         void* stream) {
+  fa_status st = check_dense(q, k, v, o, lse, B, H, Hkv, n, m, d, dv, causal, "fa_forward_fp8");
+  if (st != FA_OK) return st;
+  if (!(scale > 0.f) || scale == INFINITY)
+    return fail(FA_ERR_INVALID_ARG, "fa_forward_fp8: scale must be positive and finite");
+  if (!(q_descale > 0.f) || !(k_descale > 0.f) || !(v_descale > 0.f) || q_descale == INFINITY ||
+      k_descale == INFINITY || v_descale == INFINITY)
+    return fail(FA_ERR_INVALID_ARG, "fa_forward_fp8: descale factors must be positive and finite");
+  if (!(d == 128 && dv == 128))
+    return fail(FA_ERR_UNSUPPORTED, "fa_forward_fp8: d=%d dv=%d (supported: 128)", d, dv);
+  if (B == 0 || n == 0) return FA_OK;
+  int* sp = nullptr;
+  if ((st = status_ptr(&sp)) != FA_OK) return st;
+  fa::FwdParams p{q, k, v, o, lse, nullptr, nullptr, B, H, Hkv, n, m, d, dv, 0, 0, scale, causal,
+                  sp};
+  p.fp8 = 1;
+  p.q_descale = q_descale;
+  p.k_descale = k_descale;
+  p.v_descale = v_descale;
+  const char* why = nullptr;
+  cudaError_t e = fa::launch_fwd_bf16(p, static_cast<cudaStream_t>(stream), &why);
+  if (e != cudaSuccess) return cuda_fail(e, why ? why : "fa_forward_fp8 launch");
+  return FA_OK;
+}
+
 fa_status fa_forward_f32(const float* q, const float* k, const float* v, float* o, float* lse,
                          int B, int H, int Hkv, int n, int m, int d, int dv, float scale,
                          int causal, void* stream) {

@@ -32,6 +32,9 @@ struct FwdParams {
   const int* seq_lens = nullptr;
   int max_blocks = 0;
   int num_pages = 0;
+  // e4m3 operands (q, k, v hold x / descale), bf16 output
+  int fp8 = 0;
+  float q_descale = 1.f, k_descale = 1.f, v_descale = 1.f;
 };
 
 struct DecodeParams {

@@ -72,15 +72,22 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kPParts = 1;
 static_assert(kPParts == 1 || kPParts == 2 || kPParts == 4, "P parts");
 
-template <int D>
+// Tile geometry for head dim D and operand type (bf16, or e4m3 with FP8).
+template <int D, bool FP8 = false>
 struct Cfg {
-  static constexpr int kChunks = D / 64;                 // 64-column swizzle chunks
-  static constexpr int kTileBytes = 128 * D * 2;         // Q, K or V tile
-  static constexpr int kStages = D == 128 ? 4 : 8;       // K/V ring slots
+  static constexpr int kElem = FP8 ? 1 : 2;                 // bytes per element
+  static constexpr int kRowBytes = D * kElem;
+  static constexpr int kChunkElems = 128 / kElem;           // elements per 128-byte swizzle chunk
+  static constexpr int kChunks = kRowBytes / 128;           // chunks per row
+  static constexpr int kKStep = 32 / kElem;                 // reduction length of one MMA (32 bytes)
+  static constexpr int kTileBytes = 128 * kRowBytes;        // Q, K or V tile
+  static constexpr int kStages = kTileBytes == 32768 ? 4 : 8;   // K/V ring slots
   static constexpr int kQBytes = 2 * kTileBytes;
   static constexpr int kSmem = kQBytes + kStages * kTileBytes + 1024;  // + alignment slack
-  static constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(128, kBlockN, false, false);
-  static constexpr uint32_t kIdescO = ptx::idesc_bf16_f32(128, D, false, true);
+  static constexpr uint32_t kIdescS = FP8 ? ptx::idesc_e4m3_f32(128, kBlockN, false, false)
+                                          : ptx::idesc_bf16_f32(128, kBlockN, false, false);
+  static constexpr uint32_t kIdescO = FP8 ? ptx::idesc_e4m3_f32(128, D, false, true)
+                                          : ptx::idesc_bf16_f32(128, D, false, true);
 };
 
 struct Shared {
@@ -154,7 +161,7 @@ __device__ __forceinline__ Unit make_unit(int u, int BH, int H, int Hkv, int n, 
 // PAGED: K and V come from page caches [pages][Hkv][16][d] through the block
 // table (2-D tensor maps, one 16-row box per page), seq_lens gives each
 // sequence's key count; otherwise K/V are dense or packed rows (3-D maps).
-template <int D, bool PAGED>
+template <int D, bool PAGED, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ o,
@@ -162,8 +169,9 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 const int* __restrict__ cu_k, int B, int H, int Hkv, int n, int m, int total_q,
                 int total_k, int num_pairs, float scale_log2, int causal, int lse_stride_h,
                 int lse_stride_b, const int* __restrict__ block_table,
-                const int* __restrict__ seq_lens, int max_blocks, int num_pages, int* status) {
-  using C = Cfg<D>;
+                const int* __restrict__ seq_lens, int max_blocks, int num_pages, float out_scale,
+                int* status) {
+  using C = Cfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ Shared sh;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -257,7 +265,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             ptx::mbar_arrive_expect_tx(bar_q + 8 * i, C::kTileBytes);
 #pragma unroll
             for (int c = 0; c < C::kChunks; ++c)
-              ptx::tma_load_3d(dst + c * 16384, &tmQ, 64 * c, U.h,
+              ptx::tma_load_3d(dst + c * 16384, &tmQ, C::kChunkElems * c, U.h,
                                U.q_row0 + U.q_start0 + i * kBlockM, bar_q + 8 * i);
           }
           ++nq[i];
@@ -280,7 +288,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
               const bool fix = which == 1 && rows_valid < kBlockN;
               const uint32_t bar = fix ? bar_fix : bar_kvf + 8 * slot;
               if (lane == 0) {
-                ptx::mbar_arrive_expect_tx(bar, npages * 16 * D * 2);
+                ptx::mbar_arrive_expect_tx(bar, npages * 16 * C::kRowBytes);
                 const int* bt_row = block_table + (size_t)U.b * max_blocks + j * (kBlockN / 16);
                 for (int pg = 0; pg < npages; ++pg) {
                   int id = __ldg(bt_row + pg);
@@ -291,7 +299,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                   const int row = (id * Hkv + U.hk) * 16;
 #pragma unroll
                   for (int c = 0; c < C::kChunks; ++c)
-                    ptx::tma_load_2d(dst + c * 16384 + pg * 2048, map, 64 * c, row, bar);
+                    ptx::tma_load_2d(dst + c * 16384 + pg * 2048, map, C::kChunkElems * c, row, bar);
                 }
               }
               if (fix) {
@@ -318,7 +326,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 ptx::mbar_arrive_expect_tx(bar_kvf + 8 * slot, C::kTileBytes);
 #pragma unroll
                 for (int c = 0; c < C::kChunks; ++c)
-                  ptx::tma_load_3d(dst + c * 16384, map, 64 * c, U.hk, U.k_row0 + j * kBlockN,
+                  ptx::tma_load_3d(dst + c * 16384, map, C::kChunkElems * c, U.hk, U.k_row0 + j * kBlockN,
                                    bar_kvf + 8 * slot);
               }
             }
@@ -354,9 +362,12 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       auto issue_s = [&](int i, int slot) {
         const uint64_t kd = kdesc0 + (uint64_t)(slot * (C::kTileBytes >> 4));
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
+        for (int k = 0; k < C::kRowBytes / 32; ++k) {
           const uint32_t off = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
-          ptx::mma_ss(tbase + i * kBlockN, qdesc[i] + off, kd + off, C::kIdescS, k > 0);
+          if constexpr (FP8)
+            ptx::mma_ss_f8(tbase + i * kBlockN, qdesc[i] + off, kd + off, C::kIdescS, k > 0);
+          else
+            ptx::mma_ss(tbase + i * kBlockN, qdesc[i] + off, kd + off, C::kIdescS, k > 0);
         }
       };
       // O_i += P_i V(j) in two halves of 64 keys, each issued once the softmax
@@ -368,10 +379,16 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           if (!ptx::mbar_wait(bar_p + 8 * (kPParts * i + hf), np[i] & 1, status, abort_flag)) return false;
           ptx::tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < kBlockN / (16 * kPParts); ++kk) {
-            const int k = hf * (kBlockN / (16 * kPParts)) + kk;
-            ptx::mma_ts(tbase + 256 + i * D, tbase + i * kBlockN + k * 8, vd + (uint64_t)(k * 128),
-                        C::kIdescO, (j > 0 || k > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kBlockN / (C::kKStep * kPParts); ++kk) {
+            const int k = hf * (kBlockN / (C::kKStep * kPParts)) + kk;
+            // a step covers kKStep keys: 8 packed P columns, kKStep V rows of 128 B
+            const uint64_t bd = vd + (uint64_t)(k * C::kKStep * 8);
+            if constexpr (FP8)
+              ptx::mma_ts_f8(tbase + 256 + i * D, tbase + i * kBlockN + k * 8, bd, C::kIdescO,
+                             (j > 0 || k > 0) ? 1u : 0u);
+            else
+              ptx::mma_ts(tbase + 256 + i * D, tbase + i * kBlockN + k * 8, bd, C::kIdescO,
+                          (j > 0 || k > 0) ? 1u : 0u);
           }
         }
         ++np[i];
@@ -537,7 +554,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
         for (int a = 0; a < 4; ++a) lsum2[a] = ptx::f2_bits(0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {   // keys 32c..32c+31 -> packed columns 16c..16c+15
+        for (int c = 0; c < 4; ++c) {   // keys 32c..32c+31
+          // bf16: 2 per tensor-memory column (16 columns); e4m3: 4 per column (8)
           uint32_t pr[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
@@ -548,9 +566,22 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const float p0 = ptx::ex2(x0);
             const float p1 = ptx::ex2(x1);
             lsum2[(e / 2) & 3] = ptx::fadd2(lsum2[(e / 2) & 3], ptx::f2_bits(p0, p1));
-            pr[e / 2] = ptx::pack_bf16x2(p0, p1);
+            if constexpr (FP8) {
+              const uint32_t h = ptx::pack_e4m3x2(p0, p1);   // keys e, e+1 in the low 16 bits
+              if ((e & 2) == 0) pr[e / 4] = h;
+              else pr[e / 4] |= h << 16;
+            } else {
+              pr[e / 2] = ptx::pack_bf16x2(p0, p1);
+            }
           }
-          ptx::tmem_st16(s_col + c * 16, pr);
+          if constexpr (FP8) {
+            uint32_t p8[8];
+#pragma unroll
+            for (int w = 0; w < 8; ++w) p8[w] = pr[w];
+            ptx::tmem_st8(s_col + c * 8, p8);
+          } else {
+            ptx::tmem_st16(s_col + c * 16, pr);
+          }
           if ((c + 1) % (4 / kPParts) == 0) {   // a part is complete: hand it over
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
@@ -586,7 +617,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           for (int e = 0; e < 32; ++e) ov[c][e] = 0u;
       }
       if (row_valid) {
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        const float inv = l_run > 0.f ? out_scale / l_run : 0.f;
         uint4* dst = reinterpret_cast<uint4*>(o + orow * D);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c)
@@ -616,19 +647,20 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   }
 }
 
-template <int D, bool PAGED>
+template <int D, bool PAGED, bool FP8>
 cudaError_t launch(const FwdParams& p, cudaStream_t stream, const char** why) {
-  using C = Cfg<D>;
+  using C = Cfg<D, FP8>;
+  const CUtensorMapDataType dt = FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const bool varlen = p.cu_q != nullptr;
   // 3-D views (dim, head, token row) of Q, K, V; out-of-range rows read as 0.
   const uint64_t q_rows = varlen ? (uint64_t)(p.total_q > 0 ? p.total_q : 1) : (uint64_t)p.B * p.n;
   const uint64_t k_rows = varlen ? (uint64_t)(p.total_k > 0 ? p.total_k : 1) : (uint64_t)p.B * p.m;
   CUtensorMap tq, tk, tv;
-  const uint32_t box[3] = {64, 1, 128};
+  const uint32_t box[3] = {(uint32_t)C::kChunkElems, 1, 128};
   {
     const uint64_t dims[3] = {(uint64_t)D, (uint64_t)p.H, q_rows};
-    const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)p.H * D * 2};
-    if (!make_tmap_bf16(&tq, p.q, 3, dims, strides, box)) {
+    const uint64_t strides[2] = {(uint64_t)C::kRowBytes, (uint64_t)p.H * C::kRowBytes};
+    if (!make_tmap_bf16(&tq, p.q, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, dt)) {
       *why = "tensor map for q";
       return cudaErrorInvalidValue;
     }
@@ -636,23 +668,23 @@ cudaError_t launch(const FwdParams& p, cudaStream_t stream, const char** why) {
   if (PAGED) {
     // 2-D views (dim, page row) of the caches; one box = one page of one kv head
     const uint64_t dims[2] = {(uint64_t)D, (uint64_t)p.num_pages * p.Hkv * 16};
-    const uint64_t strides[1] = {(uint64_t)D * 2};
-    const uint32_t pbox[2] = {64, 16};
-    if (!make_tmap_bf16(&tk, p.k, 2, dims, strides, pbox) ||
-        !make_tmap_bf16(&tv, p.v, 2, dims, strides, pbox)) {
+    const uint64_t strides[1] = {(uint64_t)C::kRowBytes};
+    const uint32_t pbox[2] = {(uint32_t)C::kChunkElems, 16};
+    if (!make_tmap_bf16(&tk, p.k, 2, dims, strides, pbox, CU_TENSOR_MAP_SWIZZLE_128B, dt) ||
+        !make_tmap_bf16(&tv, p.v, 2, dims, strides, pbox, CU_TENSOR_MAP_SWIZZLE_128B, dt)) {
       *why = "tensor map for the k/v caches";
       return cudaErrorInvalidValue;
     }
   } else {
     const uint64_t dims[3] = {(uint64_t)D, (uint64_t)p.Hkv, k_rows > 0 ? k_rows : 1};
-    const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)p.Hkv * D * 2};
-    if (!make_tmap_bf16(&tk, p.m > 0 ? p.k : p.q, 3, dims, strides, box) ||
-        !make_tmap_bf16(&tv, p.m > 0 ? p.v : p.q, 3, dims, strides, box)) {
+    const uint64_t strides[2] = {(uint64_t)C::kRowBytes, (uint64_t)p.Hkv * C::kRowBytes};
+    if (!make_tmap_bf16(&tk, p.m > 0 ? p.k : p.q, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, dt) ||
+        !make_tmap_bf16(&tv, p.m > 0 ? p.v : p.q, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, dt)) {
       *why = "tensor map for k/v";
       return cudaErrorInvalidValue;
     }
   }
-  cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D, PAGED>,
+  cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D, PAGED, FP8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) {
     *why = "cudaFuncSetAttribute(fwd_bf16)";
@@ -677,12 +709,15 @@ cudaError_t launch(const FwdParams& p, cudaStream_t stream, const char** why) {
   // LSE layout: dense [B][H][n] ; varlen and paged [H][Tq]
   const int lse_stride_h = varlen ? p.total_q : p.n;
   const int lse_stride_b = varlen ? 0 : p.H * p.n;
-  const float scale_log2 = p.scale * kLog2e;
-  fwd_bf16_kernel<D, PAGED><<<grid, kThreads, C::kSmem, stream>>>(
+  // e4m3 operands hold x / descale: the q and k descales fold into the score
+  // scale, the v descale into the epilogue's 1 / l
+  const float scale_log2 = p.scale * kLog2e * (FP8 ? p.q_descale * p.k_descale : 1.f);
+  const float out_scale = FP8 ? p.v_descale : 1.f;
+  fwd_bf16_kernel<D, PAGED, FP8><<<grid, kThreads, C::kSmem, stream>>>(
       tq, tk, tv, static_cast<__nv_bfloat16*>(p.o), p.lse, p.cu_q, p.cu_k, p.B, p.H, p.Hkv, p.n,
       p.m, varlen ? p.total_q : p.B * p.n, varlen ? p.total_k : p.B * p.m, num_pairs, scale_log2,
       p.causal, lse_stride_h, lse_stride_b, p.block_table, p.seq_lens, p.max_blocks, p.num_pages,
-      p.status);
+      out_scale, p.status);
   e = cudaGetLastError();
   if (e != cudaSuccess) *why = "fwd_bf16 launch";
   return e;
@@ -692,8 +727,15 @@ cudaError_t launch(const FwdParams& p, cudaStream_t stream, const char** why) {
 
 cudaError_t launch_fwd_bf16(const FwdParams& p, cudaStream_t stream, const char** why) {
   const bool paged = p.block_table != nullptr;
-  if (p.d == 128 && p.dv == 128) return paged ? launch<128, true>(p, stream, why) : launch<128, false>(p, stream, why);
-  if (p.d == 64 && p.dv == 64) return paged ? launch<64, true>(p, stream, why) : launch<64, false>(p, stream, why);
+  if (p.fp8) {
+    if (p.d == 128 && p.dv == 128 && !paged) return launch<128, false, true>(p, stream, why);
+    *why = "fwd e4m3: supported d == dv == 128, dense or varlen";
+    return cudaErrorInvalidValue;
+  }
+  if (p.d == 128 && p.dv == 128)
+    return paged ? launch<128, true, false>(p, stream, why) : launch<128, false, false>(p, stream, why);
+  if (p.d == 64 && p.dv == 64)
+    return paged ? launch<64, true, false>(p, stream, why) : launch<64, false, false>(p, stream, why);
   *why = "fwd_bf16: unsupported head dim";
   return cudaErrorInvalidValue;
 }

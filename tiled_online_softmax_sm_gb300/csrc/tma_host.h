@@ -29,11 +29,12 @@ inline EncodeTiledFn get_encode_tiled() {
   return fn;
 }
 
-// bf16 tensor of `rank` dims (innermost first) with 128-byte swizzle.
+// bf16 (or `dtype`) tensor of `rank` dims (innermost first) with 128-byte swizzle.
 // dims/strides in elements/bytes as the driver expects (strides exclude dim 0).
 inline bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                            const uint64_t* strides_bytes, const uint32_t* box,
-                           CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+                           CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B,
+                           CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   EncodeTiledFn enc = get_encode_tiled();
   if (enc == nullptr) return false;
   cuuint64_t d[5];
@@ -46,7 +47,7 @@ inline bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const u
     e[i] = 1;
     if (i + 1 < rank) s[i] = strides_bytes[i];
   }
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base),
+  CUresult r = enc(map, dtype, (cuuint32_t)rank, const_cast<void*>(base),
                    d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;

@@ -52,13 +52,58 @@ def round_to_bf16(x: np.ndarray) -> np.ndarray:
     return bf16_bits_to_f32(f32_to_bf16_bits(x))
 
 
+def _e4m3_table():
+    """The 254 finite e4m3 (FP8, 4 exponent bits, bias 7, 3 mantissa bits) values
+    by code, NaN (0x7f, 0xff) excluded: code -> value."""
+    codes = np.arange(256, dtype=np.int64)
+    s = np.where(codes & 0x80, -1.0, 1.0)
+    e = (codes >> 3) & 0xF
+    m = codes & 0x7
+    val = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e - 7)) * s
+    finite = (codes & 0x7F) != 0x7F
+    return codes[finite], val[finite]
+
+
+_E4M3_CODES, _E4M3_VALUES = _e4m3_table()
+E4M3_MAX = 448.0
+
+
+def f32_to_e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest e4m3 value (ties to the even code), saturating at
+    +-448 (the satfinite convention); returns uint8 codes."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    pos = _E4M3_VALUES >= 0
+    pc, pv = _E4M3_CODES[pos], _E4M3_VALUES[pos]
+    order = np.argsort(pv, kind="stable")
+    pc, pv = pc[order], pv[order]
+    # +0 and -0 both appear; keep +0 (code 0) for the magnitude lookup
+    keep = np.concatenate([[True], np.diff(pv) > 0])
+    pc, pv = pc[keep], pv[keep]
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    hi = np.clip(np.searchsorted(pv, a), 1, len(pv) - 1)
+    lo = hi - 1
+    dlo, dhi = a - pv[lo], pv[hi] - a
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & ((pc[hi] & 1) == 0))
+    code = np.where(pick_hi, pc[hi], pc[lo]).astype(np.uint8)
+    code = np.where(np.signbit(x), code | 0x80, code).astype(np.uint8)
+    return code
+
+
+def e4m3_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    lut = np.zeros(256, np.float32)
+    lut[_E4M3_CODES] = _E4M3_VALUES.astype(np.float32)
+    lut[0x7F] = lut[0xFF] = np.nan
+    return lut[np.asarray(bits, dtype=np.uint8)]
+
+
 @dataclass
 class Tensor:
     """One input tensor: storage bits (bf16 as uint16, or float32) plus the
     exact float32 values the oracle reads."""
-    dtype: str            # "bf16" or "f32"
-    data: np.ndarray      # uint16 for bf16, float32 for f32
-    values: np.ndarray    # float32, exact
+    dtype: str            # "bf16", "f32" or "e4m3"
+    data: np.ndarray      # uint16 for bf16, float32 for f32, uint8 codes for e4m3
+    values: np.ndarray    # float32, exact (for e4m3: code value * descale)
+    descale: float = 1.0  # e4m3: stored value * descale = value
 
     @staticmethod
     def from_f32(x: np.ndarray, dtype: str) -> "Tensor":
@@ -68,6 +113,14 @@ class Tensor:
         if dtype == "f32":
             x = np.ascontiguousarray(x, dtype=np.float32)
             return Tensor("f32", x, x)
+        if dtype == "e4m3":
+            # per-tensor amax scaling by a power of two (so code * descale is
+            # exact in fp32): the largest magnitude lands in (224, 448]
+            amax = float(np.max(np.abs(x))) if x.size else 0.0
+            descale = float(2.0 ** np.ceil(np.log2(amax / E4M3_MAX))) if amax > 0 else 1.0
+            codes = f32_to_e4m3_bits(np.asarray(x, np.float64) / descale)
+            vals = (e4m3_bits_to_f32(codes).astype(np.float64) * descale).astype(np.float32)
+            return Tensor("e4m3", codes, vals, descale)
         raise ValueError(dtype)
 
 
