@@ -8,6 +8,8 @@ Workloads (sizes as in the bench and the parity tests):
   fwd_c2c    causal bf16 forward, B=4 H=16 n=m=2048 d=128
   varlen_c5  ragged causal bf16 varlen forward, 16 sequences, d=128
   decode_c4  paged grouped-head decode, 64 sequences, H=32 Hkv=8, 8 splits (1.3 GB KV)
+  fp8_c3     causal e4m3 forward, B=1 H=32 n=m=8192 d=128
+  prefill_c4 paged prefill: 512-token chunks of 16 sequences of the decode pool
   fwd_f32    fp32 forward, n=m=256 d=64
 Inputs come from the same seeded generators; nothing is checked here.
 """
@@ -60,6 +62,30 @@ def make(name: str, splits: int = 8):
         return lambda: fb.fa_paged_decode(q, kc, vc, bt, sl, o, lse, S, c.H, c.Hkv, c.d, c.dv,
                                           c.page_size, c.num_pages, c.max_blocks, splits, c.scale,
                                           ws, need)
+    if name == "fp8_c3":
+        g = I.rng(I.BASE_SEED, 3)
+        ts = [I.Tensor.from_f32(I.normal_f32(g, (1, 8192, 32, 128)), "e4m3") for _ in range(3)]
+        q, k, v = (torch.from_numpy(t.data).cuda() for t in ts)
+        o = torch.empty((1, 8192, 32, 128), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((1, 32, 8192), dtype=torch.float32, device="cuda")
+        sc = I.fp32_scale(128)
+        return lambda: fb.fa_forward_fp8(q, k, v, o, lse, 1, 32, 32, 8192, 8192, 128, 128, sc,
+                                         ts[0].descale, ts[1].descale, ts[2].descale, 1)
+    if name == "prefill_c4":
+        lens = I.uniform_lengths(63, 16, 512, 8192)
+        ql = np.minimum(lens, 512)
+        kv = I.decode_case(63, num_seqs=16, H=32, Hkv=8, d=128, lens=lens, max_blocks=512)
+        cu = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
+        T = int(cu[-1])
+        q = _dev(I.Tensor.from_f32(I.normal_f32(I.rng(63, 51), (T, 32, 128)), "bf16"))
+        kc, vc = _dev(kv.k_cache), _dev(kv.v_cache)
+        bt = torch.from_numpy(kv.block_table).cuda()
+        sl = torch.from_numpy(kv.seq_lens).cuda()
+        cut = torch.from_numpy(cu).cuda()
+        o = torch.empty((T, 32, 128), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((32, T), dtype=torch.float32, device="cuda")
+        return lambda: fb.fa_paged_prefill(q, kc, vc, bt, sl, cut, o, lse, 16, T, 512, 32, 8, 128,
+                                           128, 16, kv.num_pages, 512, kv.scale, 1)
     if name == "fwd_f32":
         c = I.c1_fp32()
         q, k, v = _dev(c.q), _dev(c.k), _dev(c.v)
