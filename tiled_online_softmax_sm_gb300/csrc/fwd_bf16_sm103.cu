@@ -65,12 +65,7 @@ static_assert(128 * (kProducerRegs + 2 * kSoftmaxRegs) <= kThreads * kLaunchRegs
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-// P is handed to the MMA warp in kPParts chunks of keys, each on its own
-// barrier.  Measured on GB300 (causal 8192): 1 part 1379 TFLOP/s, 2 parts
-// 1337, 4 parts 1234 -- every extra hand-off costs the single issuing thread
-// more than the overlap it buys.
-constexpr int kPParts = 1;
-static_assert(kPParts == 1 || kPParts == 2 || kPParts == 4, "P parts");
+constexpr float kRaiseSum = 256.0f;         // 2^kRescaleThreshold
 
 // Tile geometry for head dim D and operand type (bf16, or e4m3 with FP8).
 template <int D, bool FP8 = false>
@@ -94,7 +89,7 @@ struct Shared {
   uint64_t q_full[2];
   uint64_t q_empty[2];  // Q_i free for the next unit's load
   uint64_t s_full[2];
-  uint64_t p_full[2 * kPParts];   // [tile][part]
+  uint64_t p_full[2];
   uint64_t o_done[2];
   uint64_t o_empty[2];  // O_i read by the epilogue; the next unit may overwrite it
   uint64_t kv_full[8];
@@ -113,6 +108,68 @@ struct Unit {
   bool rows;       // the unit holds at least one valid query row
   bool bad;        // varlen offsets outside the buffers
 };
+
+// Row max of a 128-key S row: 8 independent chains of three-input max (one
+// chain would put 64 dependent instructions on the critical path), then a
+// small tree.
+__device__ __forceinline__ float row_max(const uint32_t (&sr)[4][32]) {
+  float mxs[8];
+#pragma unroll
+  for (int a = 0; a < 8; ++a) mxs[a] = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      const int a = (c * 16 + e / 2) & 7;
+      mxs[a] = ptx::fmax3(mxs[a], __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+    }
+  return ptx::fmax3(ptx::fmax3(mxs[0], mxs[1], mxs[2]), ptx::fmax3(mxs[3], mxs[4], mxs[5]),
+                    fmaxf(mxs[6], mxs[7]));
+}
+
+// One softmax row of a tile: p = 2^(s * scale_log2 - ref) for the 128 keys in
+// sr (nref2 holds -ref twice), written over the row's S columns as bf16 (2 per
+// tensor-memory column) or e4m3 (4 per column), with no wait for the stores.
+// Returns the row sum of p.
+template <bool FP8>
+__device__ __forceinline__ float exp_pass(const uint32_t (&sr)[4][32], uint32_t s_col,
+                                          uint64_t sc2, uint64_t nref2) {
+  uint64_t lsum2[4];   // four independent packed partial sums
+#pragma unroll
+  for (int a = 0; a < 4; ++a) lsum2[a] = ptx::f2_bits(0.f, 0.f);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {   // keys 32c..32c+31
+    uint32_t pr[16];
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      const uint64_t x = ptx::ffma2(
+          ptx::f2_bits(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])), sc2, nref2);
+      float x0, x1;
+      ptx::f2_split(x, x0, x1);
+      const float p0 = ptx::ex2(x0);
+      const float p1 = ptx::ex2(x1);
+      lsum2[(e / 2) & 3] = ptx::fadd2(lsum2[(e / 2) & 3], ptx::f2_bits(p0, p1));
+      if constexpr (FP8) {
+        const uint32_t h = ptx::pack_e4m3x2(p0, p1);   // keys e, e+1 in the low 16 bits
+        if ((e & 2) == 0) pr[e / 4] = h;
+        else pr[e / 4] |= h << 16;
+      } else {
+        pr[e / 2] = ptx::pack_bf16x2(p0, p1);
+      }
+    }
+    if constexpr (FP8) {
+      uint32_t p8[8];
+#pragma unroll
+      for (int w = 0; w < 8; ++w) p8[w] = pr[w];
+      ptx::tmem_st8(s_col + c * 8, p8);
+    } else {
+      ptx::tmem_st16(s_col + c * 16, pr);
+    }
+  }
+  float ls0, ls1;
+  ptx::f2_split(ptx::fadd2(ptx::fadd2(lsum2[0], lsum2[1]), ptx::fadd2(lsum2[2], lsum2[3])), ls0, ls1);
+  return ls0 + ls1;
+}
 
 // Units are numbered heaviest first: pair index descending, then (b, h); each
 // CTA takes them in snake order (see unit_of).
@@ -211,7 +268,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       ptx::mbar_init(bar_q + 8 * i, 1);
       ptx::mbar_init(bar_qe + 8 * i, 1);
       ptx::mbar_init(bar_s + 8 * i, 1);
-      for (int hf = 0; hf < kPParts; ++hf) ptx::mbar_init(bar_p + 8 * (kPParts * i + hf), kBlockM);
+      ptx::mbar_init(bar_p + 8 * i, kBlockM);
       ptx::mbar_init(bar_o + 8 * i, 1);
       ptx::mbar_init(bar_oe + 8 * i, kBlockM);
     }
@@ -370,26 +427,22 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             ptx::mma_ss(tbase + i * kBlockN, qdesc[i] + off, kd + off, C::kIdescS, k > 0);
         }
       };
-      // O_i += P_i V(j) in two halves of 64 keys, each issued once the softmax
-      // warps have stored that half of P; false if a wait failed
+      // O_i += P_i V(j), issued once the softmax warps have stored all of
+      // P_i; false if the wait failed
       auto issue_pv = [&](int i, int slot, int j) -> bool {
         const uint64_t vd = vdesc0 + (uint64_t)(slot * (C::kTileBytes >> 4));
+        if (!ptx::mbar_wait(bar_p + 8 * i, np[i] & 1, status, abort_flag)) return false;
+        ptx::tc_fence_after();
 #pragma unroll
-        for (int hf = 0; hf < kPParts; ++hf) {
-          if (!ptx::mbar_wait(bar_p + 8 * (kPParts * i + hf), np[i] & 1, status, abort_flag)) return false;
-          ptx::tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < kBlockN / (C::kKStep * kPParts); ++kk) {
-            const int k = hf * (kBlockN / (C::kKStep * kPParts)) + kk;
-            // a step covers kKStep keys: 8 packed P columns, kKStep V rows of 128 B
-            const uint64_t bd = vd + (uint64_t)(k * C::kKStep * 8);
-            if constexpr (FP8)
-              ptx::mma_ts_f8(tbase + 256 + i * D, tbase + i * kBlockN + k * 8, bd, C::kIdescO,
-                             (j > 0 || k > 0) ? 1u : 0u);
-            else
-              ptx::mma_ts(tbase + 256 + i * D, tbase + i * kBlockN + k * 8, bd, C::kIdescO,
-                          (j > 0 || k > 0) ? 1u : 0u);
-          }
+        for (int k = 0; k < kBlockN / C::kKStep; ++k) {
+          // a step covers kKStep keys: 8 packed P columns, kKStep V rows of 128 B
+          const uint64_t bd = vd + (uint64_t)(k * C::kKStep * 8);
+          if constexpr (FP8)
+            ptx::mma_ts_f8(tbase + 256 + i * D, tbase + i * kBlockN + k * 8, bd, C::kIdescO,
+                           (j > 0 || k > 0) ? 1u : 0u);
+          else
+            ptx::mma_ts(tbase + 256 + i * D, tbase + i * kBlockN + k * 8, bd, C::kIdescO,
+                        (j > 0 || k > 0) ? 1u : 0u);
         }
         ++np[i];
         return true;
@@ -510,88 +563,52 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             for (int e = 0; e < 32; ++e)
               if (c * 32 + e >= vis) sr[c][e] = __float_as_uint(-INFINITY);
         }
-        // row max as 8 independent chains (a single chain would be 64
-        // dependent instructions on the critical path), then a small tree
-        float mxs[8];
-#pragma unroll
-        for (int a = 0; a < 8; ++a) mxs[a] = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const int a = (c * 16 + e / 2) & 7;
-            mxs[a] = ptx::fmax3(mxs[a], __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
-          }
-        const float mx = ptx::fmax3(ptx::fmax3(mxs[0], mxs[1], mxs[2]),
-                                    ptx::fmax3(mxs[3], mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7]));
-        const float m_tile = mx * scale_log2;    // scale > 0: max commutes with it
-        const bool raise = m_tile > m_ref + kRescaleThreshold || (m_ref == -INFINITY && m_tile > -INFINITY);
-        float alpha = 1.f;
-        if (raise) {
-          alpha = m_ref == -INFINITY ? 1.f : ptx::ex2(m_ref - m_tile);
-          m_ref = m_tile;
-          l_run *= alpha;
-        }
-        const float ref = m_ref == -INFINITY ? 0.f : m_ref;
-        // rescale acc first when this warp raised a reference after the first
-        // tile: no P V of this tile may run before it
-        if (__any_sync(0xffffffffu, raise && j > 0 && alpha != 1.f)) {
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t ov[32];
-            ptx::tmem_ld32(o_col + c * 32, ov);
-            ptx::tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            ptx::tmem_st32(o_col + c * 32, ov);
-          }
-        }
-        // p = 2^(s*scale*log2e - ref), two halves of 64 keys; each half is
-        // handed to the MMA warp as soon as it sits in tensor memory
+        // From the second tile on, P is first formed against the current
+        // reference without the row max.  Every p is at most the tile's row
+        // sum, so a sum of at most 2^threshold shows that no score passed the
+        // reference by more than the threshold: no raise is due, and this P
+        // is exactly the one the max-first path forms.  Only a warp with a
+        // larger sum (or a row with no reference yet) takes the max and forms
+        // P again.
         const uint64_t sc2 = ptx::f2_bits(scale_log2, scale_log2);
-        const uint64_t nref2 = ptx::f2_bits(-ref, -ref);
-        uint64_t lsum2[4];   // four independent packed partial sums
+        float lsum = 0.f;
+        bool full = true;
+        if (j > 0) {
+          const float ref = m_ref == -INFINITY ? 0.f : m_ref;
+          lsum = exp_pass<FP8>(sr, s_col, sc2, ptx::f2_bits(-ref, -ref));
+          full = __any_sync(0xffffffffu, !(lsum <= kRaiseSum) || m_ref == -INFINITY);
+        }
+        if (full) {
+          const float m_tile = row_max(sr) * scale_log2;   // scale > 0: max commutes with it
+          const bool raise =
+              m_tile > m_ref + kRescaleThreshold || (m_ref == -INFINITY && m_tile > -INFINITY);
+          float alpha = 1.f;
+          if (raise) {
+            alpha = m_ref == -INFINITY ? 1.f : ptx::ex2(m_ref - m_tile);
+            m_ref = m_tile;
+            l_run *= alpha;
+          }
+          const float ref = m_ref == -INFINITY ? 0.f : m_ref;
+          // rescale acc when this warp raised a reference after the first
+          // tile: no P V of this tile may run before it
+          if (__any_sync(0xffffffffu, raise && j > 0 && alpha != 1.f)) {
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t ov[32];
+              ptx::tmem_ld32(o_col + c * 32, ov);
+              ptx::tmem_wait_ld();
 #pragma unroll
-        for (int a = 0; a < 4; ++a) lsum2[a] = ptx::f2_bits(0.f, 0.f);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {   // keys 32c..32c+31
-          // bf16: 2 per tensor-memory column (16 columns); e4m3: 4 per column (8)
-          uint32_t pr[16];
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const uint64_t x = ptx::ffma2(
-                ptx::f2_bits(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])), sc2, nref2);
-            float x0, x1;
-            ptx::f2_split(x, x0, x1);
-            const float p0 = ptx::ex2(x0);
-            const float p1 = ptx::ex2(x1);
-            lsum2[(e / 2) & 3] = ptx::fadd2(lsum2[(e / 2) & 3], ptx::f2_bits(p0, p1));
-            if constexpr (FP8) {
-              const uint32_t h = ptx::pack_e4m3x2(p0, p1);   // keys e, e+1 in the low 16 bits
-              if ((e & 2) == 0) pr[e / 4] = h;
-              else pr[e / 4] |= h << 16;
-            } else {
-              pr[e / 2] = ptx::pack_bf16x2(p0, p1);
+              for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+              ptx::tmem_st32(o_col + c * 32, ov);
             }
           }
-          if constexpr (FP8) {
-            uint32_t p8[8];
-#pragma unroll
-            for (int w = 0; w < 8; ++w) p8[w] = pr[w];
-            ptx::tmem_st8(s_col + c * 8, p8);
-          } else {
-            ptx::tmem_st16(s_col + c * 16, pr);
-          }
-          if ((c + 1) % (4 / kPParts) == 0) {   // a part is complete: hand it over
-            ptx::tmem_wait_st();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bar_p + 8 * (kPParts * i + c / (4 / kPParts)));
-          }
+          lsum = exp_pass<FP8>(sr, s_col, sc2, ptx::f2_bits(-ref, -ref));
         }
-        float ls0, ls1;
-        ptx::f2_split(ptx::fadd2(ptx::fadd2(lsum2[0], lsum2[1]), ptx::fadd2(lsum2[2], lsum2[3])), ls0,
-                      ls1);
-        l_run += ls0 + ls1;
+        // all of P_i sits in tensor memory: hand it to the MMA warp
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_p + 8 * i);
+        l_run += lsum;
       }
       if (!ok) break;
 
