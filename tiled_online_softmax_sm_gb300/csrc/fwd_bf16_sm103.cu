@@ -90,7 +90,14 @@ struct Cfg {
                                           : ptx::idesc_bf16_f32(128, D, false, true);
 };
 
+// Varlen and paged launches with at most this many (sequence, query pair)
+// combinations get a persistent grid over a heaviest-first list of them.
+constexpr int kMaxSortedCombos = 512;
+
 struct Shared {
+  uint16_t work[kMaxSortedCombos];    // K/V tiles of combination b * num_pairs + t
+  uint16_t order[kMaxSortedCombos];   // combinations, heaviest first
+  int n_order;                        // combinations with any work
   uint64_t q_full[2];
   uint64_t q_empty[2];  // Q_i free for the next unit's load
   uint64_t s_full[2];
@@ -176,17 +183,14 @@ __device__ __forceinline__ float exp_pass(const uint32_t (&sr)[4][32], uint32_t 
   return ls0 + ls1;
 }
 
-// Units are numbered heaviest first: pair index descending, then (b, h); each
-// CTA takes them in snake order (see unit_of).
-__device__ __forceinline__ Unit make_unit(int u, int BH, int H, int Hkv, int n, int m,
-                                          int num_pairs, int causal, const int* cu_q,
-                                          const int* cu_k, int total_q, int total_k,
-                                          const int* seq_lens, int max_blocks) {
+// The unit of query pair t (rows 256t .. 256t+255) of sequence b, head h.
+__device__ __forceinline__ Unit make_unit(int b, int h, int t, int H, int Hkv, int n, int m,
+                                          int causal, const int* cu_q, const int* cu_k,
+                                          int total_q, int total_k, const int* seq_lens,
+                                          int max_blocks) {
   Unit U;
-  const int t = num_pairs - 1 - u / BH;
-  const int bh = u % BH;
-  U.h = bh % H;
-  U.b = bh / H;
+  U.h = h;
+  U.b = b;
   U.hk = U.h / (H / Hkv);
   U.q_len = n;
   U.kv_len = m;
@@ -223,7 +227,9 @@ __device__ __forceinline__ Unit make_unit(int u, int BH, int H, int Hkv, int n, 
 // PAGED: K and V come from page caches [pages][Hkv][16][d] through the block
 // table (2-D tensor maps, one 16-row box per page), seq_lens gives each
 // sequence's key count; otherwise K/V are dense or packed rows (3-D maps).
-template <int D, bool PAGED, bool FP8>
+// VAR: varlen or paged (per-sequence lengths from device arrays); only those
+// instances carry the sorted schedule.
+template <int D, bool PAGED, bool FP8, bool VAR>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ o,
@@ -232,7 +238,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 int total_k, int num_pairs, float scale_log2, int causal, int lse_stride_h,
                 int lse_stride_b, const int* __restrict__ block_table,
                 const int* __restrict__ seq_lens, int max_blocks, int num_pages, float out_scale,
-                int* status) {
+                int sched_sorted, int* status) {
   using C = Cfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ Shared sh;
@@ -241,10 +247,50 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int BH = B * H;
-  const int num_units = BH * num_pairs;
-#define FA_UNIT(u)                                                                            \
-  make_unit((u), BH, H, Hkv, n, m, num_pairs, causal, cu_q, cu_k, total_q, total_k,              \
-            PAGED ? seq_lens : nullptr, max_blocks)
+  const int* const seq_lens_p = PAGED ? seq_lens : nullptr;
+  auto unit_bt = [&](int b, int h, int t) {
+    return make_unit(b, h, t, H, Hkv, n, m, causal, cu_q, cu_k, total_q, total_k, seq_lens_p,
+                     max_blocks);
+  };
+  // Dense: units are numbered heaviest first, pair index descending, then
+  // (b, h).  Sorted (varlen and paged, few combinations): every CTA builds the
+  // same list of (sequence, pair) combinations ordered by K/V tiles
+  // descending (ties by index), and unit u is head u % H of entry u / H.
+  if (VAR && sched_sorted) {
+    const int C = B * num_pairs;
+    if (threadIdx.x == 0) sh.n_order = 0;
+    __syncthreads();
+    for (int c = threadIdx.x; c < C; c += blockDim.x) {
+      const Unit U = unit_bt(c / num_pairs, 0, c % num_pairs);
+      if (U.bad) atomicExch(status, kDevInvalidArg);  // skipped, touches nothing
+      // a unit with query rows but no keys still writes O = 0 and LSE = -inf
+      sh.work[c] = (uint16_t)(U.rows ? 1 + U.n_kv[0] + U.n_kv[1] : 0);
+    }
+    __syncthreads();
+    int mine = 0;
+    for (int c = threadIdx.x; c < C; c += blockDim.x) {
+      const int w = sh.work[c];
+      int rank = 0;
+      for (int c2 = 0; c2 < C; ++c2) {
+        const int w2 = sh.work[c2];
+        rank += (w2 > w) || (w2 == w && c2 < c);
+      }
+      sh.order[rank] = (uint16_t)c;
+      mine += w > 0;
+    }
+    if (mine) atomicAdd(&sh.n_order, mine);
+    __syncthreads();
+  }
+  const int num_units = VAR && sched_sorted ? H * sh.n_order : BH * num_pairs;
+  auto unit_at = [&](int u) {
+    if (VAR && sched_sorted) {
+      const int c = sh.order[u / H];
+      return unit_bt(c / num_pairs, u % H, c % num_pairs);
+    }
+    const int bh = u % BH;
+    return unit_bt(bh / H, bh % H, num_pairs - 1 - u / BH);
+  };
+#define FA_UNIT(u) unit_at(u)
   // k-th unit of this CTA: waves of gridDim.x units in snake order (even waves
   // left to right, odd waves right to left), which evens out the per-CTA sum
   // of the heaviest-first unit sizes
@@ -712,28 +758,25 @@ cudaError_t launch(const FwdParams& p, cudaStream_t stream, const char** why) {
       return cudaErrorInvalidValue;
     }
   }
-  cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D, PAGED, FP8>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-  if (e != cudaSuccess) {
-    *why = "cudaFuncSetAttribute(fwd_bf16)";
-    return e;
-  }
   const int num_pairs = (p.n + 2 * kBlockM - 1) / (2 * kBlockM);
   const long long units = (long long)p.B * p.H * num_pairs;
   int sms = 0;
   {
     int dev = 0;
+    cudaError_t e;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
         (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) {
       *why = "query SM count";
       return e;
     }
   }
-  // Dense: persistent, one CTA per SM (the shared-memory footprint admits
-  // one), units in snake order.  Varlen and paged: one CTA per unit, so the
-  // hardware block scheduler balances units whose sizes depend on lengths
-  // the host does not know (idle units exit at once).
-  const int grid = varlen ? (int)units : (int)(units < sms ? units : sms);
+  // Persistent, one CTA per SM (the shared-memory footprint admits one),
+  // units in snake order: dense, and varlen or paged with few (sequence,
+  // pair) combinations (the kernel sorts them by size).  Otherwise one CTA
+  // per unit, so the hardware block scheduler balances units whose sizes
+  // depend on lengths the host does not know (idle units exit at once).
+  const bool sorted = varlen && (long long)p.B * num_pairs <= kMaxSortedCombos;
+  const int grid = varlen && !sorted ? (int)units : (int)(units < sms ? units : sms);
   // LSE layout: dense [B][H][n] ; varlen and paged [H][Tq]
   const int lse_stride_h = varlen ? p.total_q : p.n;
   const int lse_stride_b = varlen ? 0 : p.H * p.n;
@@ -741,14 +784,23 @@ cudaError_t launch(const FwdParams& p, cudaStream_t stream, const char** why) {
   // scale, the v descale into the epilogue's 1 / l
   const float scale_log2 = p.scale * kLog2e * (FP8 ? p.q_descale * p.k_descale : 1.f);
   const float out_scale = FP8 ? p.v_descale : 1.f;
-  fwd_bf16_kernel<D, PAGED, FP8><<<grid, kThreads, C::kSmem, stream>>>(
-      tq, tk, tv, static_cast<__nv_bfloat16*>(p.o), p.lse, p.cu_q, p.cu_k, p.B, p.H, p.Hkv, p.n,
-      p.m, varlen ? p.total_q : p.B * p.n, varlen ? p.total_k : p.B * p.m, num_pairs, scale_log2,
-      p.causal, lse_stride_h, lse_stride_b, p.block_table, p.seq_lens, p.max_blocks, p.num_pages,
-      out_scale, p.status);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) *why = "fwd_bf16 launch";
-  return e;
+  auto go = [&](auto kernel) -> cudaError_t {
+    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (err != cudaSuccess) {
+      *why = "cudaFuncSetAttribute(fwd_bf16)";
+      return err;
+    }
+    kernel<<<grid, kThreads, C::kSmem, stream>>>(
+        tq, tk, tv, static_cast<__nv_bfloat16*>(p.o), p.lse, p.cu_q, p.cu_k, p.B, p.H, p.Hkv, p.n,
+        p.m, varlen ? p.total_q : p.B * p.n, varlen ? p.total_k : p.B * p.m, num_pairs, scale_log2,
+        p.causal, lse_stride_h, lse_stride_b, p.block_table, p.seq_lens, p.max_blocks, p.num_pages,
+        out_scale, sorted ? 1 : 0, p.status);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) *why = "fwd_bf16 launch";
+    return err;
+  };
+  if constexpr (PAGED) return go(fwd_bf16_kernel<D, true, FP8, true>);
+  else return varlen ? go(fwd_bf16_kernel<D, false, FP8, true>) : go(fwd_bf16_kernel<D, false, FP8, false>);
 }
 
 }  // namespace
