@@ -22,13 +22,15 @@
 //   execute in issue order.
 //
 // Per K/V tile a softmax thread loads its S row, masks (causal diagonal tile,
-// keys past the sequence end), takes the row max in log2 units
-// (s * scale * log2 e), and forms p = 2^(s - ref).  The reference ref is the
-// running max, raised only when a tile's max exceeds it by more than 8 (a
-// factor 256): then acc (O in tensor memory) and l are multiplied by
-// alpha = 2^(m_old - m_new) before the next P V.  Between raises p can reach
-// 256, which bf16 and fp32 hold exactly enough; the final O = acc / l and
-// LSE = (ref + log2 l) ln 2 are exact in any case.  While a row has seen only
+// keys past the sequence end) and forms p = 2^(s - ref) in log2 units
+// (s * scale * log2 e).  The reference ref is the running max, raised only
+// when a tile's max exceeds it by more than 8 (a factor 256): then acc (O in
+// tensor memory) and l are multiplied by alpha = 2^(m_old - m_new) before the
+// next P V.  Between raises p can reach 256, which bf16 and fp32 hold exactly
+// enough; the final O = acc / l and LSE = (ref + log2 l) ln 2 are exact in
+// any case.  The row max itself is taken only when needed: p is first formed
+// against the current ref, and a tile row sum of at most 256 proves no raise
+// is due (see the softmax loop).  While a row has seen only
 // masked keys its reference is 0, so exp(-inf - -inf) never occurs ("S12
 // FlashAttention", 实现).  Whole K/V tiles above the causal diagonal are never
 // loaded or multiplied ("手搓 Attention" §6).  Causal is aligned bottom-right:
