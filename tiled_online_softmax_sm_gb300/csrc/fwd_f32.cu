@@ -4,9 +4,10 @@
 // "S12 FlashAttention" (解法), one CTA per (batch, head, block of query rows):
 //   - the CTA keeps its query rows in registers and streams K/V tiles of
 //     kTileN rows through shared memory, one tile live at a time;
-//   - four threads share a query row; each owns a quarter of d (for Q·K) and a
-//     quarter of dv (for the accumulator), interleaved in float4 chunks so
-//     that the four lanes of a row read adjacent 16-byte words of a K/V row;
+//   - kThreadsPerRow lanes share a query row; each owns d/kThreadsPerRow of
+//     the dimensions (for Q·K) and dv/kThreadsPerRow (for the accumulator),
+//     interleaved in float4 chunks so that the lanes of a row read adjacent
+//     16-byte words of a K/V row;
 //   - per tile: raw dot products q·k_j carried as compensated pairs, tile
 //     max, m_new, the rescale alpha = exp(scale·(m - m_new)) and
 //     p_j = exp(scale·(s_j - m_new)), both evaluated as 2^(x·log2 e); whole
@@ -21,9 +22,12 @@
 namespace fa {
 namespace {
 
-constexpr int kRowsPerCta = 32;                 // query rows per CTA
-constexpr int kThreadsPerRow = 4;
-constexpr int kThreads = kRowsPerCta * kThreadsPerRow;  // 128
+// Lanes of a warp sharing a query row.  The kernel is bound by latency (a
+// 256-row problem is only 256 rows): measured on GB300 at n = m = 256, d = 64,
+// 4 lanes 92 us, 8 lanes 66 us, 16 lanes 60 us per launch.
+constexpr int kThreadsPerRow = 16;
+constexpr int kThreads = 128;
+constexpr int kRowsPerCta = kThreads / kThreadsPerRow;  // query rows per CTA
 constexpr int kTileN = 32;                      // keys per K/V tile
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -81,15 +85,17 @@ fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
   const int i = q0 + row;                       // query index of this row
   const bool row_valid = i < n;
 
-  constexpr int QC = D / 16;    // float4 chunks of q owned by this thread
-  constexpr int VC = DV / 16;   // float4 chunks of acc owned by this thread
+  constexpr int QC = D / (4 * kThreadsPerRow);    // float4 chunks of q owned by this thread
+  constexpr int VC = DV / (4 * kThreadsPerRow);   // float4 chunks of acc owned by this thread
+  static_assert(QC >= 1 && VC >= 1, "a thread owns at least one float4 of q and of acc");
 
   float4 qr[QC];
   float4 acc[VC];
   {
     const float4* qrow = reinterpret_cast<const float4*>(q + (((size_t)b * n + (row_valid ? i : 0)) * H + h) * D);
 #pragma unroll
-    for (int c = 0; c < QC; ++c) qr[c] = row_valid ? qrow[c * 4 + part] : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = 0; c < QC; ++c)
+      qr[c] = row_valid ? qrow[c * kThreadsPerRow + part] : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int c = 0; c < VC; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
@@ -132,7 +138,7 @@ fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
       float hi = 0.f, lo = 0.f;
 #pragma unroll
       for (int c = 0; c < QC; ++c) {
-        const float4 kk = kr[c * 4 + part];
+        const float4 kk = kr[c * kThreadsPerRow + part];
         dot2_step(qr[c].x, kk.x, hi, lo);
         dot2_step(qr[c].y, kk.y, hi, lo);
         dot2_step(qr[c].z, kk.z, hi, lo);
@@ -174,7 +180,7 @@ fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
       const float4* vr = sV + j * (DV / 4);
 #pragma unroll
       for (int c = 0; c < VC; ++c) {
-        const float4 vv = vr[c * 4 + part];
+        const float4 vv = vr[c * kThreadsPerRow + part];
         acc[c].x = fmaf(p, vv.x, acc[c].x);
         acc[c].y = fmaf(p, vv.y, acc[c].y);
         acc[c].z = fmaf(p, vv.z, acc[c].z);
@@ -192,7 +198,7 @@ fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
 #pragma unroll
   for (int c = 0; c < VC; ++c) {
     const float4 x = acc[c];
-    orow[c * 4 + part] = make_float4(x.x * inv, x.y * inv, x.z * inv, x.w * inv);
+    orow[c * kThreadsPerRow + part] = make_float4(x.x * inv, x.y * inv, x.z * inv, x.w * inv);
   }
   if (lse != nullptr && part == 0)
     lse[((size_t)b * H + h) * n + i] =
