@@ -26,8 +26,19 @@ namespace {
 // 256-row problem is only 256 rows): measured on GB300 at n = m = 256, d = 64,
 // 4 lanes 92 us, 8 lanes 66 us, 16 lanes 60 us per launch.
 constexpr int kThreadsPerRow = 16;
-constexpr int kThreads = 128;
-constexpr int kRowsPerCta = kThreads / kThreadsPerRow;  // query rows per CTA
+constexpr int kGroupThreads = 128;                          // one key group
+constexpr int kRowsPerCta = kGroupThreads / kThreadsPerRow;  // query rows per CTA
+// The CTA's key tiles are dealt to kGroups groups of 128 threads (tile t to
+// group t % kGroups), each with its own rows' state and tile buffer, and the
+// groups' (max, sum, acc) are merged at the end the way split partials are
+// ("S12 FlashAttention", 它还解锁了什么): a row's key tiles run side by side.
+constexpr int kGroups = 4;
+constexpr int kThreads = kGroupThreads * kGroups;
+
+// bar.sync on a named barrier of the kGroupThreads threads of one group
+__device__ __forceinline__ void group_sync(int group) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(kGroupThreads) : "memory");
+}
 constexpr int kTileN = 32;                      // keys per K/V tile
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -71,11 +82,12 @@ fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
                const float* __restrict__ v, float* __restrict__ o, float* __restrict__ lse,
                int B, int H, int Hkv, int n, int m, float scale, int causal) {
   extern __shared__ float4 smem4[];
-  float4* sK = smem4;                           // [kTileN][D/4]
-  float4* sV = smem4 + kTileN * (D / 4);        // [kTileN][DV/4]
+  const int group = threadIdx.x / kGroupThreads;
+  const int tid = threadIdx.x % kGroupThreads;   // thread within its group
+  float4* sK = smem4 + group * kTileN * ((D + DV) / 4);   // [kTileN][D/4] of this group
+  float4* sV = sK + kTileN * (D / 4);                     // [kTileN][DV/4]
 
   const float scale_log2 = scale * kLog2e;
-  const int tid = threadIdx.x;
   const int row = tid / kThreadsPerRow;
   const int part = tid % kThreadsPerRow;
   const int h = blockIdx.y;
@@ -111,20 +123,20 @@ fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
   const float* kbase = k + ((size_t)b * m * Hkv + hk) * D;
   const float* vbase = v + ((size_t)b * m * Hkv + hk) * DV;
 
-  for (int j0 = 0; j0 < kv_end; j0 += kTileN) {
+  for (int j0 = group * kTileN; j0 < kv_end; j0 += kGroups * kTileN) {
     const int cols = min(kTileN, m - j0);
-    __syncthreads();  // previous tile fully consumed
-    for (int idx = tid; idx < kTileN * (D / 4); idx += kThreads) {
+    group_sync(group);  // previous tile fully consumed
+    for (int idx = tid; idx < kTileN * (D / 4); idx += kGroupThreads) {
       int r = idx / (D / 4), c = idx % (D / 4);
       sK[idx] = r < cols ? reinterpret_cast<const float4*>(kbase + (size_t)(j0 + r) * k_row_stride)[c]
                          : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    for (int idx = tid; idx < kTileN * (DV / 4); idx += kThreads) {
+    for (int idx = tid; idx < kTileN * (DV / 4); idx += kGroupThreads) {
       int r = idx / (DV / 4), c = idx % (DV / 4);
       sV[idx] = r < cols ? reinterpret_cast<const float4*>(vbase + (size_t)(j0 + r) * v_row_stride)[c]
                          : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    __syncthreads();
+    group_sync(group);
 
     int vis = cols;                 // visible keys of this row in the tile: [0, vis)
     if (causal) vis = min(vis, i + off - j0 + 1);
@@ -192,6 +204,52 @@ fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
     m_lo = n_lo;
   }
 
+  // ---- merge the groups: each publishes (max pair, sum, acc) of its rows;
+  // group 0 rescales them to the common max and adds them up
+  __syncthreads();   // every group is done with its tile buffer
+  float* st = reinterpret_cast<float*>(smem4);   // [kGroups][kRowsPerCta][4 + DV]
+  constexpr int kRowFloats = 4 + DV;   // max pair, sum, a pad word: acc stays 16-byte aligned
+  float* mine = st + (group * kRowsPerCta + row) * kRowFloats;
+  if (part == 0) {
+    mine[0] = m_hi;
+    mine[1] = m_lo;
+    mine[2] = l_run;
+  }
+#pragma unroll
+  for (int c = 0; c < VC; ++c)
+    reinterpret_cast<float4*>(mine + 4)[c * kThreadsPerRow + part] = acc[c];
+  __syncthreads();
+  if (group != 0) return;
+  float g_hi = -INFINITY, g_lo = 0.f;   // max over the groups
+  for (int g = 0; g < kGroups; ++g) {
+    const float* o_g = st + (g * kRowsPerCta + row) * kRowFloats;
+    if (o_g[0] > g_hi) {
+      g_hi = o_g[0];
+      g_lo = o_g[1];
+    }
+  }
+  l_run = 0.f;
+#pragma unroll
+  for (int c = 0; c < VC; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (g_hi != -INFINITY) {
+    for (int g = 0; g < kGroups; ++g) {
+      const float* o_g = st + (g * kRowsPerCta + row) * kRowFloats;
+      if (o_g[0] == -INFINITY) continue;   // this group saw no key of the row
+      const float w = exp2f(pair_diff_scaled(o_g[0], o_g[1], g_hi, g_lo, scale_log2));
+      l_run = fmaf(w, o_g[2], l_run);
+#pragma unroll
+      for (int c = 0; c < VC; ++c) {
+        const float4 a = reinterpret_cast<const float4*>(o_g + 4)[c * kThreadsPerRow + part];
+        acc[c].x = fmaf(w, a.x, acc[c].x);
+        acc[c].y = fmaf(w, a.y, acc[c].y);
+        acc[c].z = fmaf(w, a.z, acc[c].z);
+        acc[c].w = fmaf(w, a.w, acc[c].w);
+      }
+    }
+  }
+  m_hi = g_hi;
+  m_lo = g_lo;
+
   if (!row_valid) return;
   const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
   float4* orow = reinterpret_cast<float4*>(o + (((size_t)b * n + i) * H + h) * DV);
@@ -207,7 +265,9 @@ fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
 
 template <int D, int DV>
 cudaError_t launch(const FwdParams& p, cudaStream_t stream) {
-  const size_t smem = sizeof(float) * kTileN * (D + DV);
+  const size_t tiles = sizeof(float) * kTileN * (D + DV) * kGroups;
+  const size_t merge = sizeof(float) * kGroups * kRowsPerCta * (4 + DV);
+  const size_t smem = tiles > merge ? tiles : merge;
   cudaError_t e = cudaFuncSetAttribute(fwd_f32_kernel<D, DV>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
