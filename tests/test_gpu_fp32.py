@@ -39,6 +39,10 @@ def test_c1_single_head_256(hot):
     (1, 1, 1, 5, 333, 64, 64, False),
     (1, 2, 1, 40, 130, 64, 64, True),
     (2, 2, 2, 130, 40, 128, 128, True),
+    # several key tiles per key group, ragged last tile; and the causal
+    # diagonal crossing the groups' tiles
+    (1, 2, 2, 64, 1000, 64, 64, False),
+    (1, 2, 1, 700, 700, 64, 128, True),
 ])
 def test_fp32_shapes(shape):
     B, H, Hkv, n, m, d, dv, causal = shape
