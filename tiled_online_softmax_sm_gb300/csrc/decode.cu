@@ -45,6 +45,7 @@ constexpr int kD = 128;             // head dim (d == dv)
 // splits (193-195 us, 0.89 of the measured HBM copy bandwidth); 4 x 4 gave
 // 209 us, 4 x 3 199 us, 2 x 8 361 us.
 constexpr int kWarps = 4;           // units per CTA
+constexpr int kMaxRankedSeqs = 256;  // launches with more sequences keep index order
 constexpr int kStages = 2;          // pages in flight per warp
 constexpr int kHalfBytes = kPage * 64 * 2;     // one 64-column swizzled half page: 2 KB
 constexpr int kPageBytes = 2 * kHalfBytes;     // 4 KB (K or V of one page and kv head)
@@ -87,11 +88,29 @@ decode_partials_kernel(const __grid_constant__ CUtensorMap tmK,
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int unit = blockIdx.x * kWarps + warp;
+  // Longest sequences first: CTAs start in block order, so a grid whose
+  // heavy units come last ends on a long tail.  With few sequences every CTA
+  // ranks them by length (ties by index) in shared memory; unit u then
+  // belongs to the (u / (X * Hkv))-th longest.
+  __shared__ int s_len[kMaxRankedSeqs];
+  __shared__ int s_order[kMaxRankedSeqs];
+  const bool ranked = num_seqs <= kMaxRankedSeqs;
+  if (ranked) {
+    for (int t = threadIdx.x; t < num_seqs; t += blockDim.x) s_len[t] = seq_lens[t];
+    __syncthreads();
+    for (int t = threadIdx.x; t < num_seqs; t += blockDim.x) {
+      const int Lt = s_len[t];
+      int rank = 0;
+      for (int u = 0; u < num_seqs; ++u) rank += (s_len[u] > Lt) || (s_len[u] == Lt && u < t);
+      s_order[rank] = t;
+    }
+    __syncthreads();
+  }
   if (unit >= num_seqs * Hkv * X) return;
 
   const int x = unit % X;
   const int g = (unit / X) % Hkv;
-  const int s = unit / (X * Hkv);
+  const int s = ranked ? s_order[unit / (X * Hkv)] : unit / (X * Hkv);
   const int G = H / Hkv;
   const int L = seq_lens[s];
   const int P = L > 0 ? (L + kPage - 1) / kPage : 0;
