@@ -472,7 +472,7 @@ def run_ours(args, world, rank, local):
                    "frac_of_hbm_peak": round(dec_achieved / peaks["hbm_gbs"], 4)},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-                     "traffic": tr_fwd, "kernel": "fwd_bf16_kernel<128, false, false>",
+                     "traffic": tr_fwd, "kernel": "fwd_bf16_kernel<128, false, false, false>",
                      "peak_source": f"{peaks['source']} bf16 burst",
                      "flops_per_launch": flops},
         "roofline_decode": {"bound": "hbm", "achieved": round(dec_achieved, 2),
