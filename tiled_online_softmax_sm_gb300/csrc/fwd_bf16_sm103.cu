@@ -397,20 +397,22 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
               // a V tile reaching past the end lands on the fix barrier first
               const bool fix = which == 1 && rows_valid < kBlockN;
               const uint32_t bar = fix ? bar_fix : bar_kvf + 8 * slot;
-              if (lane == 0) {
-                ptx::mbar_arrive_expect_tx(bar, npages * 16 * C::kRowBytes);
-                const int* bt_row = block_table + (size_t)U.b * max_blocks + j * (kBlockN / 16);
-                for (int pg = 0; pg < npages; ++pg) {
-                  int id = __ldg(bt_row + pg);
-                  if (id < 0 || id >= num_pages) {
-                    atomicExch(status, kDevBadBlockTable);
-                    id = 0;
-                  }
-                  const int row = (id * Hkv + U.hk) * 16;
-#pragma unroll
-                  for (int c = 0; c < C::kChunks; ++c)
-                    ptx::tma_load_2d(dst + c * 16384 + pg * 2048, map, C::kChunkElems * c, row, bar);
+              // lane 0 posts the byte count (the barrier's one arrival, so the
+              // phase cannot complete before it), then lane pg looks up page
+              // pg and issues its boxes: the page copies go out in parallel
+              if (lane == 0) ptx::mbar_arrive_expect_tx(bar, npages * 16 * C::kRowBytes);
+              __syncwarp();
+              if (lane < npages) {
+                const int pg = lane;
+                int id = __ldg(block_table + (size_t)U.b * max_blocks + j * (kBlockN / 16) + pg);
+                if (id < 0 || id >= num_pages) {
+                  atomicExch(status, kDevBadBlockTable);
+                  id = 0;
                 }
+                const int row = (id * Hkv + U.hk) * 16;
+#pragma unroll
+                for (int c = 0; c < C::kChunks; ++c)
+                  ptx::tma_load_2d(dst + c * 16384 + pg * 2048, map, C::kChunkElems * c, row, bar);
               }
               if (fix) {
                 fix_pending = true;
