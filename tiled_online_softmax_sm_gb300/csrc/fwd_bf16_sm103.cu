@@ -355,6 +355,10 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         ptx::prefetch_tmap(&tmK);
         ptx::prefetch_tmap(&tmV);
       }
+      // Q is read once; K and V are read again by the other query-tile pairs
+      // of the head, so they are the ones L2 should keep
+      const uint64_t pol_q = ptx::policy_evict_first();
+      const uint64_t pol_kv = ptx::policy_evict_last();
       int li = 0;                 // K/V loads issued (K(j), V(j) alternate)
       int nq[2] = {0, 0};         // Q loads issued per tile
       int nfix = 0;               // V tiles zero-fixed (paged)
@@ -375,8 +379,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             ptx::mbar_arrive_expect_tx(bar_q + 8 * i, C::kTileBytes);
 #pragma unroll
             for (int c = 0; c < C::kChunks; ++c)
-              ptx::tma_load_3d(dst + c * 16384, &tmQ, C::kChunkElems * c, U.h,
-                               U.q_row0 + U.q_start0 + i * kBlockM, bar_q + 8 * i);
+              ptx::tma_load_3d_hint(dst + c * 16384, &tmQ, C::kChunkElems * c, U.h,
+                                    U.q_row0 + U.q_start0 + i * kBlockM, bar_q + 8 * i, pol_q);
           }
           ++nq[i];
         }
@@ -438,8 +442,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 ptx::mbar_arrive_expect_tx(bar_kvf + 8 * slot, C::kTileBytes);
 #pragma unroll
                 for (int c = 0; c < C::kChunks; ++c)
-                  ptx::tma_load_3d(dst + c * 16384, map, C::kChunkElems * c, U.hk, U.k_row0 + j * kBlockN,
-                                   bar_kvf + 8 * slot);
+                  ptx::tma_load_3d_hint(dst + c * 16384, map, C::kChunkElems * c, U.hk,
+                                        U.k_row0 + j * kBlockN, bar_kvf + 8 * slot, pol_kv);
               }
             }
             ++li;
