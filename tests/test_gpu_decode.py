@@ -113,9 +113,12 @@ def test_bad_block_id_sets_status_without_fault():
     assert_close(host(o)[0], o_ref[0], BF16_MAX_ABS, BF16_MEAN_ABS)
 
 
-def test_split_combine_against_oracle_merge():
-    rng = I.rng(11)
-    S, H, X, dv = 3, 4, 6, 128
+@pytest.mark.parametrize("X, dv", [(6, 128), (1, 64), (33, 64), (64, 256), (40, 96)])
+def test_split_combine_against_oracle_merge(X, dv):
+    """Merge of arbitrary partials: splits past 32 (two per lane), the 64-split
+    limit, and head dims that leave lanes idle (64, 96) or take two chunks."""
+    rng = I.rng(11, X, dv)
+    S, H = 3, 4
     pm = rng.normal(size=(S, H, X)) * 5
     pm[0, 0, :] = -np.inf                  # all empty
     pm[1, 2, ::2] = -np.inf                # some empty

@@ -319,8 +319,13 @@ split_combine_kernel(const float* __restrict__ part_m, const float* __restrict__
   if (t >= pairs) return;
   const float* pm = part_m + (size_t)t * X;
   const float* pl = part_l + (size_t)t * X;
-  float M = -INFINITY;
-  for (int x = 0; x < X; ++x) M = fmaxf(M, __ldg(pm + x));
+  // lane x holds split x and x + 32 (X <= 64): the weights are computed once
+  // and handed out by shuffles, so the o loads below are all independent
+  const float m0 = lane < X ? __ldg(pm + lane) : -INFINITY;
+  const float m1 = lane + 32 < X ? __ldg(pm + lane + 32) : -INFINITY;
+  float M = fmaxf(m0, m1);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   __nv_bfloat16* orow = o + (size_t)t * dv;
   if (M == -INFINITY) {
     for (int c = lane * 4; c < dv; c += 128) {
@@ -329,28 +334,43 @@ split_combine_kernel(const float* __restrict__ part_m, const float* __restrict__
     if (lane == 0 && lse != nullptr) lse[t] = -INFINITY;
     return;
   }
-  float l = 0.f;
-  for (int x = 0; x < X; ++x) {
-    const float mx = __ldg(pm + x);
-    const float w = mx == -INFINITY ? 0.f : exp2f((mx - M) * kLog2e);
-    l += w * __ldg(pl + x);
-  }
+  const float w0 = m0 == -INFINITY ? 0.f : exp2f((m0 - M) * kLog2e);
+  const float w1 = m1 == -INFINITY ? 0.f : exp2f((m1 - M) * kLog2e);
+  float l = (lane < X ? w0 * __ldg(pl + lane) : 0.f) + (lane + 32 < X ? w1 * __ldg(pl + lane + 32) : 0.f);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
   const float inv = l > 0.f ? 1.f / l : 0.f;
-  for (int c = lane * 4; c < dv; c += 128) {
+  const float* po = part_o + (size_t)t * X * dv;
+  // every lane runs every chunk (the shuffles need the whole warp); lanes
+  // past dv load and store nothing
+  for (int c0 = 0; c0 < dv; c0 += 128) {
+    const int c = c0 + lane * 4;
+    const bool active = c < dv;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int x = 0; x < X; ++x) {
-      const float mx = __ldg(pm + x);
-      const float w = mx == -INFINITY ? 0.f : exp2f((mx - M) * kLog2e);
-      const float4 v = __ldg(reinterpret_cast<const float4*>(part_o + ((size_t)t * X + x) * dv + c));
-      acc.x = fmaf(w, v.x, acc.x);
-      acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z);
-      acc.w = fmaf(w, v.w, acc.w);
+    for (int x0 = 0; x0 < X; x0 += 8) {
+      float4 v[8];
+      float w[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int x = x0 + u;
+        w[u] = __shfl_sync(0xffffffffu, x < 32 ? w0 : w1, x & 31);
+        v[u] = active && x < X ? __ldg(reinterpret_cast<const float4*>(po + (size_t)x * dv + c))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        acc.x = fmaf(w[u], v[u].x, acc.x);
+        acc.y = fmaf(w[u], v[u].y, acc.y);
+        acc.z = fmaf(w[u], v[u].z, acc.z);
+        acc.w = fmaf(w[u], v[u].w, acc.w);
+      }
     }
-    uint2 packed;
-    packed.x = ptx::pack_bf16x2(acc.x * inv, acc.y * inv);
-    packed.y = ptx::pack_bf16x2(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2*>(orow + c) = packed;
+    if (active) {
+      uint2 packed;
+      packed.x = ptx::pack_bf16x2(acc.x * inv, acc.y * inv);
+      packed.y = ptx::pack_bf16x2(acc.z * inv, acc.w * inv);
+      *reinterpret_cast<uint2*>(orow + c) = packed;
+    }
   }
   if (lane == 0 && lse != nullptr) lse[t] = l > 0.f ? M + logf(l) : -INFINITY;
 }
