@@ -807,8 +807,17 @@ cudaError_t launch(const FwdParams& p, cudaStream_t stream, const char** why) {
     if (err != cudaSuccess) *why = "fwd_bf16 launch";
     return err;
   };
-  if constexpr (PAGED) return go(fwd_bf16_kernel<D, true, FP8, true>);
-  else return varlen ? go(fwd_bf16_kernel<D, false, FP8, true>) : go(fwd_bf16_kernel<D, false, FP8, false>);
+  if constexpr (PAGED) {
+    return go(fwd_bf16_kernel<D, true, FP8, true>);
+  } else if constexpr (FP8) {   // the C ABI's e4m3 entry is dense only
+    if (varlen) {
+      *why = "fwd e4m3: dense only";
+      return cudaErrorInvalidValue;
+    }
+    return go(fwd_bf16_kernel<D, false, true, false>);
+  } else {
+    return varlen ? go(fwd_bf16_kernel<D, false, false, true>) : go(fwd_bf16_kernel<D, false, false, false>);
+  }
 }
 
 }  // namespace
@@ -817,7 +826,7 @@ cudaError_t launch_fwd_bf16(const FwdParams& p, cudaStream_t stream, const char*
   const bool paged = p.block_table != nullptr;
   if (p.fp8) {
     if (p.d == 128 && p.dv == 128 && !paged) return launch<128, false, true>(p, stream, why);
-    *why = "fwd e4m3: supported d == dv == 128, dense or varlen";
+    *why = "fwd e4m3: supported d == dv == 128, dense";
     return cudaErrorInvalidValue;
   }
   if (p.d == 128 && p.dv == 128)
