@@ -77,6 +77,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* st
   }
 }
 
+// ------------------------------------------------- tensor copies (TMA)
+// 2-D / 3-D tiled copies global -> shared, completion counted on an mbarrier.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y,
                                             uint32_t bar) {
   asm volatile(
