@@ -257,6 +257,34 @@ def test_recurrence_guard_fully_masked_first_tiles():
     np.testing.assert_allclose(l_rec, l_def[0, 0], rtol=0, atol=1e-12)
 
 
+def test_unguarded_recurrence_reproduces_the_nan_trap():
+    """Negative control for the guard above ("S12 FlashAttention", 实现 and 练习
+    2): the same diagonal-first visit order with the textbook update
+    m_new = max(m, tile max), alpha = exp(m - m_new), p = exp(s - m_new),
+    written test-side without the guard, turns early rows into NaN."""
+    n = m = 32
+    q, k, v = _rand(33, n, 8), _rand(34, m, 8), _rand(35, m, 8)
+    s = (q.astype(np.float64) @ k.astype(np.float64).T) * 0.5
+    s[np.triu_indices(n, 1)] = -np.inf                  # causal: j <= i
+    blocks = [slice(16, 32), slice(0, 16)]               # future block first
+    m_run = np.full(n, -np.inf)
+    l_run = np.zeros(n)
+    acc = np.zeros((n, 8))
+    with np.errstate(invalid="ignore"):
+        for blk in blocks:
+            st = s[:, blk]
+            m_new = np.maximum(m_run, st.max(axis=1))
+            alpha = np.exp(m_run - m_new)                # -inf - -inf = NaN for early rows
+            p = np.exp(st - m_new[:, None])
+            l_run = alpha * l_run + p.sum(axis=1)
+            acc = alpha[:, None] * acc + p @ v[blk].astype(np.float64)
+            m_run = m_new
+    o_naive = acc / l_run[:, None]
+    assert np.isnan(o_naive[:16]).all()                  # rows 0..15 see nothing in block 1
+    o_rec, _ = oracle.online_recurrence(q, k, v, 0.5, True, q_block=16, kv_block=16, kv_order=[1, 0])
+    assert np.isfinite(o_rec).all()
+
+
 # ----------------------------------------------------------------------------
 # Paged decode, split partials and their merge
 # ----------------------------------------------------------------------------
