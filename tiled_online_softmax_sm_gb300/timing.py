@@ -1,0 +1,165 @@
+"""Device timing of every workload of the hot path, one table.
+
+  python -m tiled_online_softmax_sm_gb300.timing [--iters 20] [--warmup 5]
+
+Each workload runs on resident inputs from the seeded generators (the same
+as the tests and the bench).  A row reports the median of `iters` timed
+launches after `warmup` untimed ones, each launch between CUDA events on the
+launching stream.  The fp32 workload is tiny and its launches are timed as
+20 back-to-back launches captured in a CUDA graph (per-launch median), so the
+host call does not show up as device time.  Rates use nominal work:
+4*n*m*d*H*B FLOPs (halved when causal; the ragged and paged rows sum their
+sequences), and for the decode the K and V bytes of every valid token.
+Nothing is checked here; parity lives in the tests.
+"""
+from __future__ import annotations
+
+import argparse
+import sys
+
+import numpy as np
+import torch
+
+from . import binding as fb
+from . import inputs as I
+
+
+def _dev(t):
+    if t.dtype == "bf16":
+        return torch.from_numpy(t.data.view(np.int16)).cuda().view(torch.bfloat16)
+    return torch.from_numpy(t.data).cuda()
+
+
+def _median_ms(fn, iters, warmup):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(iters):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return float(np.median(ts))
+
+
+def _graph_median_ms(fn, iters, warmup, per_graph=20):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(per_graph):
+            fn()
+    return _median_ms(g.replay, iters, 3) / per_graph
+
+
+def _dense(c, iters, warmup):
+    q, k, v = _dev(c.q), _dev(c.k), _dev(c.v)
+    o = torch.empty((c.B, c.n, c.H, c.dv), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((c.B, c.H, c.n), dtype=torch.float32, device="cuda")
+    ms = _median_ms(lambda: fb.fa_forward(q, k, v, o, lse, c.B, c.H, c.Hkv, c.n, c.m, c.d, c.dv,
+                                          c.scale, int(c.causal)), iters, warmup)
+    flops = 4.0 * c.n * c.m * c.d * c.H * c.B / (2 if c.causal else 1)
+    return ms, flops / (ms * 1e9), "TFLOP/s"
+
+
+def rows(iters: int, warmup: int):
+    out = []
+    c = I.c1_fp32()
+    q, k, v = _dev(c.q), _dev(c.k), _dev(c.v)
+    o = torch.empty((c.B, c.n, c.H, c.dv), dtype=torch.float32, device="cuda")
+    lse = torch.empty((c.B, c.H, c.n), dtype=torch.float32, device="cuda")
+    ms = _graph_median_ms(lambda: fb.fa_forward_f32(q, k, v, o, lse, c.B, c.H, c.Hkv, c.n, c.m,
+                                                    c.d, c.dv, c.scale, 0), iters, warmup)
+    out.append(("fp32 n=m=256 d=64 (graph replay)", ms, 4.0 * c.n * c.m * c.d / (ms * 1e9), "TFLOP/s"))
+    for causal in (False, True):
+        out.append((f"bf16 B=4 H=16 n=m=2048 d=128 causal={causal}",) + _dense(I.c2_bf16(causal=causal), iters, warmup))
+    out.append(("bf16 B=1 H=32 n=m=8192 d=128 causal",) + _dense(I.c3_bf16(), iters, warmup))
+    # e4m3 forward, same long-context shape
+    g = I.rng(I.BASE_SEED, 3)
+    ts = [I.Tensor.from_f32(I.normal_f32(g, (1, 8192, 32, 128)), "e4m3") for _ in range(3)]
+    q8, k8, v8 = (torch.from_numpy(t.data).cuda() for t in ts)
+    o8 = torch.empty((1, 8192, 32, 128), dtype=torch.bfloat16, device="cuda")
+    l8 = torch.empty((1, 32, 8192), dtype=torch.float32, device="cuda")
+    ms = _median_ms(lambda: fb.fa_forward_fp8(q8, k8, v8, o8, l8, 1, 32, 32, 8192, 8192, 128, 128,
+                                              I.fp32_scale(128), ts[0].descale, ts[1].descale,
+                                              ts[2].descale, 1), iters, warmup)
+    out.append(("e4m3 B=1 H=32 n=m=8192 d=128 causal", ms, 4.0 * 8192 * 8192 * 128 * 32 / 2 / (ms * 1e9), "TFLOP/s"))
+    del q8, k8, v8, o8, l8
+    # paged grouped-head decode at 4, 8, 16 splits
+    dc = I.c4_decode(poison=False)
+    qd, kc, vc = _dev(dc.q), _dev(dc.k_cache), _dev(dc.v_cache)
+    bt = torch.from_numpy(dc.block_table).cuda()
+    sl = torch.from_numpy(dc.seq_lens).cuda()
+    S = len(dc.seq_lens)
+    for X in (4, 8, 16):
+        need = fb.fa_paged_decode_workspace_size(S, dc.H, dc.dv, X)
+        ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+        od = torch.empty((S, dc.H, dc.dv), dtype=torch.bfloat16, device="cuda")
+        ld = torch.empty((S, dc.H), dtype=torch.float32, device="cuda")
+        ms = _median_ms(lambda: fb.fa_paged_decode(qd, kc, vc, bt, sl, od, ld, S, dc.H, dc.Hkv, dc.d,
+                                                   dc.dv, dc.page_size, dc.num_pages, dc.max_blocks,
+                                                   X, dc.scale, ws, need), iters, warmup)
+        out.append((f"paged decode 64 seqs H=32 Hkv=8 splits={X}", ms, dc.kv_bytes / (ms * 1e6), "GB/s"))
+    # paged prefill: 512-token chunks of 16 sequences of the decode pool
+    lens = I.uniform_lengths(63, 16, 512, 8192)
+    ql = np.minimum(lens, 512)
+    kv = I.decode_case(63, num_seqs=16, H=32, Hkv=8, d=128, lens=lens, max_blocks=512, poison=False)
+    cu = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
+    T = int(cu[-1])
+    qp = _dev(I.Tensor.from_f32(I.normal_f32(I.rng(63, 51), (T, 32, 128)), "bf16"))
+    kp, vp = _dev(kv.k_cache), _dev(kv.v_cache)
+    btp = torch.from_numpy(kv.block_table).cuda()
+    slp = torch.from_numpy(kv.seq_lens).cuda()
+    cut = torch.from_numpy(cu).cuda()
+    op = torch.empty((T, 32, 128), dtype=torch.bfloat16, device="cuda")
+    lp = torch.empty((32, T), dtype=torch.float32, device="cuda")
+    ms = _median_ms(lambda: fb.fa_paged_prefill(qp, kp, vp, btp, slp, cut, op, lp, 16, T, 512, 32, 8,
+                                                128, 128, 16, kv.num_pages, 512, kv.scale, 1),
+                    iters, warmup)
+    fl = sum(4.0 * int(nq) * 128 * 32 * (int(L) - int(nq) / 2) for nq, L in zip(ql, lens))
+    out.append(("paged prefill 16 x 512-token chunks H=32 Hkv=8", ms, fl / (ms * 1e9), "TFLOP/s"))
+    # ragged causal varlen
+    for d in (64, 128):
+        vcase = I.c5_varlen(d)
+        qv, kvv, vv = _dev(vcase.q), _dev(vcase.k), _dev(vcase.v)
+        cuv = torch.from_numpy(vcase.cu_seqlens).cuda()
+        Tv = int(vcase.cu_seqlens[-1])
+        mx = int(vcase.lens.max())
+        ov = torch.empty((Tv, vcase.H, vcase.dv), dtype=torch.bfloat16, device="cuda")
+        lv = torch.empty((vcase.H, Tv), dtype=torch.float32, device="cuda")
+        ms = _median_ms(lambda: fb.fa_forward_varlen(qv, kvv, vv, ov, lv, cuv, cuv, len(vcase.lens), Tv,
+                                                     Tv, mx, mx, vcase.H, vcase.Hkv, d, d, vcase.scale,
+                                                     1), iters, warmup)
+        fl = sum(4.0 * int(L) * int(L) * d * vcase.H / 2 for L in vcase.lens)
+        out.append((f"ragged causal varlen 16 seqs H=16 d={d}", ms, fl / (ms * 1e9), "TFLOP/s"))
+    return out
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--iters", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    a = ap.parse_args(argv)
+    print(f"| workload | median time | rate |\n|---|---|---|")
+    for name, ms, rate, unit in rows(a.iters, a.warmup):
+        t = f"{ms * 1000:.1f} us" if ms < 1 else f"{ms:.3f} ms"
+        print(f"| {name} | {t} | {rate:.1f} {unit} |", flush=True)
+    st = fb.fa_get_device_status()
+    if st != 0:
+        print(f"device status {st}")
+        return 1
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
