@@ -4,10 +4,13 @@
 
 Each workload runs on resident inputs from the seeded generators (the same
 as the tests and the bench).  A row reports the median of `iters` timed
-launches after `warmup` untimed ones, each launch between CUDA events on the
-launching stream.  The fp32 workload is tiny and its launches are timed as
-20 back-to-back launches captured in a CUDA graph (per-launch median), so the
-host call does not show up as device time.  Rates use nominal work:
+launches after `warmup` untimed ones.  The launches are queued back to back
+on the current stream with a CUDA event between each pair, so every interval
+is one launch's device time and not the host's call.  The fp32 workload is
+tiny (its device time is below the host's call time) and is timed as graph
+replays of 20 launches, per launch.  Inputs smaller than L2 (the n=m=2048
+shapes, the fp32 case) stay L2-resident across launches; the long-context,
+decode, prefill and ragged inputs are larger than L2.  Rates use nominal work:
 4*n*m*d*H*B FLOPs (halved when causal; the ragged and paged rows sum their
 sequences), and for the decode the K and V bytes of every valid token.
 Nothing is checked here; parity lives in the tests.
@@ -31,19 +34,18 @@ def _dev(t):
 
 
 def _median_ms(fn, iters, warmup):
+    # Launches are queued back to back with an event between each pair, so
+    # the device never waits for the host's call and each interval is one
+    # launch's device time; the warm-up launches are queued ahead of them.
     for _ in range(warmup):
         fn()
-    torch.cuda.synchronize()
-    ts = []
-    for _ in range(iters):
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(iters + 1)]
+    evs[0].record()
+    for i in range(iters):
         fn()
-        b.record()
-        torch.cuda.synchronize()
-        ts.append(a.elapsed_time(b))
-    return float(np.median(ts))
+        evs[i + 1].record()
+    torch.cuda.synchronize()
+    return float(np.median([evs[i].elapsed_time(evs[i + 1]) for i in range(iters)]))
 
 
 def _graph_median_ms(fn, iters, warmup, per_graph=20):
