@@ -195,7 +195,9 @@ size_t fa_paged_decode_workspace_size(int num_seqs, int H, int dv, int num_split
  *                and then merges them (fa_split_combine) on the same stream.
  * Tokens past seq_len in the last page are never used (their cache contents
  * may be anything, NaN included).  Page ids are range-checked on the device:
- * an id outside [0, num_pages) is skipped and sets FA_ERR_BAD_BLOCK_TABLE.
+ * an id outside [0, num_pages) is skipped and sets FA_ERR_BAD_BLOCK_TABLE.  A
+ * seq_lens[s] outside [0, max_blocks_per_seq*page_size] is treated as an
+ * empty sequence (O = 0, LSE = -inf) and sets FA_ERR_INVALID_ARG.
  * Supported: d == dv == 128, page_size == 16, H / Hkv <= 16.
  */
 fa_status fa_paged_decode(const void* q, const void* k_cache, const void* v_cache,
@@ -234,6 +236,30 @@ fa_status fa_paged_decode_noalloc(const void* q, const void* k_cache, const void
                                   float* lse, int num_seqs, int H, int Hkv, int d, int dv,
                                   int page_size, int num_pages, int max_blocks_per_seq,
                                   int num_splits, float scale, void* stream);
+
+/*
+ * fa_paged_gather — checking tool for the block-table walk of fa_paged_decode.
+ * Passage: "S12 FlashAttention", 实现 (logical page p of sequence s is
+ * physical page block_table[s][p] and holds min(page_size, seq_len -
+ * p*page_size) valid tokens).
+ *
+ * Runs the decode's units (sequence, kv head, split) with the decode's split
+ * page ranges, page lookups, tensor copies and shared-memory page layout, and
+ * copies the K and V rows it gathers out to dense buffers instead of scoring
+ * them, so a test can compare them bit for bit with a host gather.
+ *   k_cache, v_cache, block_table, seq_lens, num_pages, max_blocks_per_seq,
+ *   num_splits   as fa_paged_decode
+ *   k_out, v_out bf16 [num_seqs][max_blocks_per_seq*page_size][Hkv][d],
+ *                caller-owned: token t of sequence s is written to row
+ *                s*max_blocks_per_seq*page_size + t for t < seq_lens[s]; other
+ *                rows are not written.
+ * Device status as fa_paged_decode (bad page ids, out-of-range seq_lens).
+ * Supported: d == 128, page_size == 16.
+ */
+fa_status fa_paged_gather(const void* k_cache, const void* v_cache, const int* block_table,
+                          const int* seq_lens, void* k_out, void* v_out, int num_seqs, int Hkv,
+                          int d, int page_size, int num_pages, int max_blocks_per_seq,
+                          int num_splits, void* stream);
 
 /*
  * fa_split_combine — merge per-split partial triples with the recurrence's

@@ -2,7 +2,9 @@
 
 Against the float64 oracle: O max-abs 2e-2 and mean-abs 2e-3, LSE 1e-3.
 Block-table indexing is checked bit-exactly: the same kernel on the same KV
-laid out contiguously behind an identity table must give identical bits.
+laid out contiguously behind an identity table must give identical bits, and
+the decode's page walk gathered out to dense buffers (fa_paged_gather) must
+equal a host gather bit for bit.
 Unused pool pages and the tail slots of each last page hold NaN, so a stray
 read shows up as NaN in O.
 """
@@ -111,6 +113,78 @@ def test_bad_block_id_sets_status_without_fault():
     # the untouched sequence is still right
     o_ref, _ = _oracle(case)
     assert_close(host(o)[0], o_ref[0], BF16_MAX_ABS, BF16_MEAN_ABS)
+
+
+def test_out_of_range_seq_len_sets_status_and_reads_nothing():
+    """A length past the block table's row (or below zero) is caught on the
+    device: the sequence counts as empty (O = 0, LSE = -inf), the status word
+    says FA_ERR_INVALID_ARG, and the other sequences are unaffected."""
+    case = I.decode_case(11, num_seqs=3, H=8, Hkv=2, d=128, lens=[40, 40, 40], max_blocks=4)
+    lens = case.seq_lens.copy()
+    lens[1] = 4 * 16 + 1
+    lens[2] = -5
+    o, lse = fb.paged_decode(dev(case.q), dev(case.k_cache), dev(case.v_cache),
+                             dev_i32(case.block_table), dev_i32(lens), 2, case.scale)
+    assert fb.fa_get_device_status() == fb.FA_ERR_INVALID_ARG
+    oh, lh = host(o), host(lse)
+    assert (oh[1:] == 0).all() and np.isneginf(lh[1:]).all()
+    o_ref, lse_ref = _oracle(case)
+    assert_close(oh[0], o_ref[0], BF16_MAX_ABS, BF16_MEAN_ABS)
+    assert_lse_close(lh[0], lse_ref[0])
+
+
+# ---- the decode's page walk, gathered out: bit-exact against a host gather
+
+_SENTINEL = 0x1234   # a finite bf16 pattern no gathered row is compared against
+
+
+def _gpu_gather(case, splits):
+    S, maxb = case.block_table.shape
+    Hkv = case.k_cache.data.shape[1]
+    ko = torch.full((S, maxb * 16, Hkv, 128), _SENTINEL, dtype=torch.int16, device="cuda")
+    vo = torch.full_like(ko, _SENTINEL)
+    fb.fa_paged_gather(dev(case.k_cache), dev(case.v_cache), dev_i32(case.block_table),
+                       dev_i32(case.seq_lens), ko, vo, S, Hkv, 128, 16, case.num_pages, maxb,
+                       splits)
+    return ko, vo
+
+
+def _host_gather(case, s):
+    """Token t of sequence s is slot t % 16 of physical page block_table[s, t // 16]."""
+    t = np.arange(int(case.seq_lens[s]))
+    pages = case.block_table[s, t // 16]
+    return case.k_cache.data[pages, :, t % 16, :], case.v_cache.data[pages, :, t % 16, :]
+
+
+def _check_gathered(case, ko, vo, seqs):
+    for s in seqs:
+        L = int(case.seq_lens[s])
+        k_ref, v_ref = _host_gather(case, s)
+        kg = ko[s].cpu().numpy().view(np.uint16)
+        vg = vo[s].cpu().numpy().view(np.uint16)
+        assert np.array_equal(kg[:L], k_ref), f"K rows of sequence {s}"
+        assert np.array_equal(vg[:L], v_ref), f"V rows of sequence {s}"
+        assert (kg[L:] == _SENTINEL).all() and (vg[L:] == _SENTINEL).all(), f"rows past {L}"
+
+
+@pytest.mark.parametrize("splits", [1, 3, 8, 64])
+def test_gathered_rows_equal_host_gather(splits):
+    """Split page ranges, page lookups, tensor-copy rows and the swizzled page
+    layout of the decode give exactly the rows the block table names; nothing
+    past seq_len (NaN-poisoned in the cache) is written."""
+    lens = [0, 1, 15, 16, 17, 100, 257, 640]
+    case = I.decode_case(5, num_seqs=len(lens), H=32, Hkv=8, d=128, lens=lens, max_blocks=48)
+    ko, vo = _gpu_gather(case, splits)
+    _check_gathered(case, ko, vo, range(len(lens)))
+    assert fb.fa_get_device_status() == 0
+
+
+def test_gathered_rows_full_size_pool():
+    """The 64-sequence pool (contexts 512..8192) at 8 splits, sampled sequences."""
+    case = I.c4_decode()
+    ko, vo = _gpu_gather(case, 8)
+    _check_gathered(case, ko, vo, [0, 17, 40, 63])
+    assert fb.fa_get_device_status() == 0
 
 
 @pytest.mark.parametrize("X, dv", [(6, 128), (1, 64), (33, 64), (64, 256), (40, 96)])

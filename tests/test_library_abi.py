@@ -102,6 +102,27 @@ def test_decode_validation(lib):
     assert _dec(lib, S=0) == fb.FA_OK
 
 
+def _gather(lib, **kw):
+    a = dict(kc=16, vc=16, bt=16, sl=16, ko=16, vo=16, S=4, Hkv=8, d=128, page=16, P=100, maxb=8,
+             X=4)
+    a.update(kw)
+    return lib.fa_paged_gather(a["kc"], a["vc"], a["bt"], a["sl"], a["ko"], a["vo"], a["S"],
+                               a["Hkv"], a["d"], a["page"], a["P"], a["maxb"], a["X"], None)
+
+
+def test_gather_validation(lib):
+    assert _gather(lib, X=0) == fb.FA_ERR_INVALID_ARG
+    assert _gather(lib, X=65) == fb.FA_ERR_INVALID_ARG
+    assert _gather(lib, Hkv=0) == fb.FA_ERR_INVALID_ARG
+    assert _gather(lib, S=-1) == fb.FA_ERR_INVALID_ARG
+    assert _gather(lib, d=64) == fb.FA_ERR_UNSUPPORTED
+    assert _gather(lib, page=32) == fb.FA_ERR_UNSUPPORTED
+    assert _gather(lib, ko=None) == fb.FA_ERR_INVALID_ARG
+    assert _gather(lib, vo=24) == fb.FA_ERR_INVALID_ARG          # not 16-byte aligned
+    assert _gather(lib, P=0) == fb.FA_ERR_INVALID_ARG
+    assert _gather(lib, S=0) == fb.FA_OK
+
+
 def test_combine_validation(lib):
     assert lib.fa_split_combine(16, 16, 16, 16, 16, 4, 8, 0, 128, None) == fb.FA_ERR_INVALID_ARG
     assert lib.fa_split_combine(16, 16, 16, 16, 16, 4, 8, 4, 130, None) == fb.FA_ERR_UNSUPPORTED

@@ -30,7 +30,8 @@ FA_ERR_BAD_BLOCK_TABLE = 6
 
 EXPORTED = ("fa_forward", "fa_forward_fp8", "fa_forward_f32", "fa_forward_varlen", "fa_paged_prefill",
             "fa_paged_decode_workspace_size",
-            "fa_paged_decode", "fa_paged_decode_noalloc", "fa_split_combine", "fa_last_error",
+            "fa_paged_decode", "fa_paged_decode_noalloc", "fa_paged_gather", "fa_split_combine",
+            "fa_last_error",
             "fa_get_device_status")
 FA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -65,6 +66,7 @@ def load(path: str = LIB_PATH):
         lib.fa_paged_decode_workspace_size.restype = Z
         lib.fa_paged_decode.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, P, Z, P]
         lib.fa_paged_decode_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, P]
+        lib.fa_paged_gather.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, P]
         lib.fa_split_combine.argtypes = [P, P, P, P, P, I, I, I, I, P]
         lib.fa_last_error.argtypes = []
         lib.fa_last_error.restype = ctypes.c_char_p
@@ -72,7 +74,8 @@ def load(path: str = LIB_PATH):
         for name in ("fa_forward", "fa_forward_fp8", "fa_forward_f32", "fa_forward_varlen",
                      "fa_paged_prefill",
                      "fa_paged_decode",
-                     "fa_paged_decode_noalloc", "fa_split_combine", "fa_get_device_status"):
+                     "fa_paged_decode_noalloc", "fa_paged_gather", "fa_split_combine",
+                     "fa_get_device_status"):
             getattr(lib, name).restype = I
         _lib = lib
         return lib
@@ -161,6 +164,13 @@ def fa_paged_decode_noalloc(q, k_cache, v_cache, block_table, seq_lens, o, lse, 
                                           _p(seq_lens), _p(o), _p(lse), num_seqs, H, Hkv, d, dv,
                                           page_size, num_pages, max_blocks_per_seq, num_splits,
                                           float(scale), _stream(stream)))
+
+
+def fa_paged_gather(k_cache, v_cache, block_table, seq_lens, k_out, v_out, num_seqs, Hkv, d,
+                    page_size, num_pages, max_blocks_per_seq, num_splits, stream=None):
+    _check(load().fa_paged_gather(_p(k_cache), _p(v_cache), _p(block_table), _p(seq_lens),
+                                  _p(k_out), _p(v_out), num_seqs, Hkv, d, page_size, num_pages,
+                                  max_blocks_per_seq, num_splits, _stream(stream)))
 
 
 def fa_split_combine(part_m, part_l, part_o, o, lse, num_seqs, H, num_splits, dv, stream=None):

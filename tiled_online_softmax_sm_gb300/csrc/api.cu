@@ -296,6 +296,37 @@ fa_status fa_paged_decode(const void* q, const void* k_cache, const void* v_cach
   return FA_OK;
 }
 
+fa_status fa_paged_gather(const void* k_cache, const void* v_cache, const int* block_table,
+                          const int* seq_lens, void* k_out, void* v_out, int num_seqs, int Hkv,
+                          int d, int page_size, int num_pages, int max_blocks_per_seq,
+                          int num_splits, void* stream) {
+  const char* fn = "fa_paged_gather";
+  if (num_seqs < 0 || num_pages < 0 || max_blocks_per_seq < 0)
+    return fail(FA_ERR_INVALID_ARG, "%s: negative size", fn);
+  if (Hkv <= 0) return fail(FA_ERR_INVALID_ARG, "%s: Hkv=%d", fn, Hkv);
+  if (num_splits < 1 || num_splits > 64)
+    return fail(FA_ERR_INVALID_ARG, "%s: num_splits=%d outside [1, 64]", fn, num_splits);
+  if (d != 128) return fail(FA_ERR_UNSUPPORTED, "%s: d=%d (supported: 128)", fn, d);
+  if (page_size != 16) return fail(FA_ERR_UNSUPPORTED, "%s: page_size=%d (supported: 16)", fn, page_size);
+  if (num_seqs == 0) return FA_OK;
+  if (k_cache == nullptr || v_cache == nullptr || block_table == nullptr || seq_lens == nullptr ||
+      k_out == nullptr || v_out == nullptr)
+    return fail(FA_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (num_pages == 0 || max_blocks_per_seq == 0)
+    return fail(FA_ERR_INVALID_ARG, "%s: empty page pool or block table", fn);
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_out) || !aligned16(v_out) ||
+      (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return fail(FA_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
+  int* sp = nullptr;
+  fa_status st = status_ptr(&sp);
+  if (st != FA_OK) return st;
+  fa::GatherParams p{k_cache, v_cache, block_table, seq_lens, k_out, v_out,
+                     num_seqs, Hkv, num_pages, max_blocks_per_seq, num_splits, sp};
+  cudaError_t e = fa::launch_decode_gather(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fa_paged_gather launch");
+  return FA_OK;
+}
+
 fa_status fa_split_combine(const float* part_m, const float* part_l, const float* part_o, void* o,
                            float* lse, int num_seqs, int H, int num_splits, int dv, void* stream) {
   const char* fn = "fa_split_combine";

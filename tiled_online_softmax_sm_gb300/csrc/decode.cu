@@ -24,6 +24,10 @@
 //
 // split_combine_kernel — one warp per (sequence, head): M = max m_x,
 //   w_x = exp(m_x - M), O = sum w_x o_x / sum w_x l_x, LSE = M + ln l.
+//
+// decode_gather_kernel — a checking tool for the block-table walk: the
+//   decode's units, page ranges, lookups, tensor copies and swizzled page
+//   layout, with the gathered K and V rows copied out to dense buffers.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -76,6 +80,23 @@ __device__ __forceinline__ int page_id(const int* bt_row, int p, int num_pages, 
   return bad ? 0 : id;
 }
 
+// A sequence length outside [0, max_blocks * 16] would walk past its row of
+// the block table: it is recorded (FA_ERR_INVALID_ARG) and the sequence is
+// treated as empty.
+__device__ __forceinline__ int checked_len(int L, int max_blocks, int* status, int lane) {
+  if (L >= 0 && (long long)L <= (long long)max_blocks * kPage) return L;
+  if (lane == 0) atomicExch(status, kDevInvalidArg);
+  return 0;
+}
+
+// Pages [pb, pe) of split x of X over a sequence of L tokens: page-aligned,
+// near-equal, ceil(x P / X) .. ceil((x + 1) P / X) for P = ceil(L / 16).
+__device__ __forceinline__ void split_pages(int x, int X, int L, int& pb, int& pe) {
+  const int P = L > 0 ? (L + kPage - 1) / kPage : 0;
+  pb = (int)(((long long)x * P + X - 1) / X);
+  pe = (int)(((long long)(x + 1) * P + X - 1) / X);
+}
+
 __global__ void __launch_bounds__(kWarps * 32)
 decode_partials_kernel(const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
@@ -112,10 +133,9 @@ decode_partials_kernel(const __grid_constant__ CUtensorMap tmK,
   const int g = (unit / X) % Hkv;
   const int s = ranked ? s_order[unit / (X * Hkv)] : unit / (X * Hkv);
   const int G = H / Hkv;
-  const int L = seq_lens[s];
-  const int P = L > 0 ? (L + kPage - 1) / kPage : 0;
-  const int pb = (int)(((long long)x * P + X - 1) / X);
-  const int pe = (int)(((long long)(x + 1) * P + X - 1) / X);
+  const int L = checked_len(seq_lens[s], max_blocks, status, lane);
+  int pb, pe;
+  split_pages(x, X, L, pb, pe);
   const int* bt_row = block_table + (size_t)s * max_blocks;
 
   const uint32_t ring = ptx::smem_u32(smem + warp * kStages * kStageBytes);
@@ -375,6 +395,73 @@ split_combine_kernel(const float* __restrict__ part_m, const float* __restrict__
   if (lane == 0 && lse != nullptr) lse[t] = l > 0.f ? M + logf(l) : -INFINITY;
 }
 
+// Block-table check: the decode's units (one warp per sequence, kv head and
+// split, in index order), each walking its split's pages with the decode's
+// range rule (split_pages), lookups (page_id) and tensor copies (issue_page)
+// into the same 128-byte-swizzled page layout, then copying the valid rows out
+// of shared memory (swz) to dense K and V buffers [num_seqs][max_blocks * 16]
+// [Hkv][128]: token t of sequence s lands on row s * max_blocks * 16 + t.
+// Rows at or past seq_len are not written.  One page in flight per warp.
+constexpr int kGatherSmemBytes = kWarps * kStageBytes + kWarps * 8 + 1024;  // + alignment slack
+
+__global__ void __launch_bounds__(kWarps * 32)
+decode_gather_kernel(const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const int* __restrict__ block_table,
+                     const int* __restrict__ seq_lens, int num_seqs, int Hkv, int num_pages,
+                     int max_blocks, int X, __nv_bfloat16* __restrict__ k_out,
+                     __nv_bfloat16* __restrict__ v_out, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int unit = blockIdx.x * kWarps + warp;
+  if (unit >= num_seqs * Hkv * X) return;
+  const int x = unit % X;
+  const int g = (unit / X) % Hkv;
+  const int s = unit / (X * Hkv);
+  const int L = checked_len(seq_lens[s], max_blocks, status, lane);
+  int pb, pe;
+  split_pages(x, X, L, pb, pe);
+  const int* bt_row = block_table + (size_t)s * max_blocks;
+  const uint8_t* stage = smem + warp * kStageBytes;
+  const uint32_t stage_a = ptx::smem_u32(stage);
+  const uint32_t bar = ptx::smem_u32(smem + kWarps * kStageBytes) + warp * 8;
+  if (lane == 0) {
+    ptx::mbar_init(bar, 1);
+    ptx::fence_mbar_init();
+  }
+  __syncwarp();
+  const size_t row0 = (size_t)s * max_blocks * kPage;
+  for (int p = pb; p < pe; ++p) {
+    bool bad;
+    const int id = page_id(bt_row, p, num_pages, bad);
+    if (lane == 0) {
+      if (bad) atomicExch(status, kDevBadBlockTable);
+      ptx::fence_proxy_async_smem();   // the previous page's reads come before this copy
+      issue_page(&tmK, &tmV, stage_a, bar, id, Hkv, g);
+    }
+    if (!__all_sync(0xffffffffu, ptx::mbar_wait(bar, (p - pb) & 1, status))) {
+      // the copy may still land: let it (bounded) before the warp leaves
+      if (lane == 0) ptx::mbar_wait(bar, (p - pb) & 1, nullptr);
+      __syncwarp();
+      return;
+    }
+    const int nvalid = bad ? 0 : min(kPage, L - p * kPage);
+    // 16-byte units: K rows then V rows, 16 units (two swizzled halves) per row
+    for (int idx = lane; idx < 2 * nvalid * 16; idx += 32) {
+      const int which = idx / (nvalid * 16);
+      const int rem = idx - which * nvalid * 16;
+      const int row = rem >> 4, u = rem & 15;
+      const uint4 val = *reinterpret_cast<const uint4*>(stage + which * kPageBytes +
+                                                        (u >> 3) * kHalfBytes + swz(row, u & 7));
+      __nv_bfloat16* out = which ? v_out : k_out;
+      *reinterpret_cast<uint4*>(out + ((row0 + (size_t)p * kPage + row) * Hkv + g) * kD + u * 8) = val;
+    }
+    __syncwarp();
+  }
+}
+
 // Failure-detection test hook: FA_TEST_FORCE_WAIT_TIMEOUT=1 in the
 // environment makes every decode warp skip its first page copy, so its
 // bounded wait expires (after ~1 s), FA_ERR_TIMEOUT is recorded and the warp
@@ -405,6 +492,25 @@ cudaError_t launch_decode_partials(const DecodeParams& p, cudaStream_t stream) {
       tmK, tmV, static_cast<const __nv_bfloat16*>(p.q), p.block_table, p.seq_lens, p.num_seqs,
       p.H, p.Hkv, p.num_pages, p.max_blocks, p.num_splits, p.scale * kLog2e, p.part_m, p.part_l,
       p.part_o, p.status, skip_first_copy_for_tests());
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_gather(const GatherParams& p, cudaStream_t stream) {
+  if (p.num_seqs == 0) return cudaSuccess;
+  CUtensorMap tmK, tmV;
+  const uint64_t rows = (uint64_t)p.num_pages * p.Hkv * kPage;
+  const uint64_t dims[2] = {(uint64_t)kD, rows};
+  const uint64_t strides[1] = {(uint64_t)kD * 2};
+  const uint32_t box[2] = {64, (uint32_t)kPage};
+  if (!make_tmap_bf16(&tmK, p.k_cache, 2, dims, strides, box) ||
+      !make_tmap_bf16(&tmV, p.v_cache, 2, dims, strides, box))
+    return cudaErrorInvalidValue;
+  const int units = p.num_seqs * p.Hkv * p.num_splits;
+  const int grid = (units + kWarps - 1) / kWarps;
+  decode_gather_kernel<<<grid, kWarps * 32, kGatherSmemBytes, stream>>>(
+      tmK, tmV, p.block_table, p.seq_lens, p.num_seqs, p.Hkv, p.num_pages, p.max_blocks,
+      p.num_splits, static_cast<__nv_bfloat16*>(p.k_out), static_cast<__nv_bfloat16*>(p.v_out),
+      p.status);
   return cudaGetLastError();
 }
 

@@ -60,9 +60,21 @@ struct CombineParams {
   int num_seqs, H, num_splits, dv;
 };
 
+struct GatherParams {
+  const void* k_cache;
+  const void* v_cache;
+  const int* block_table;
+  const int* seq_lens;
+  void* k_out;         // bf16 [S][max_blocks * 16][Hkv][128]
+  void* v_out;
+  int num_seqs, Hkv, num_pages, max_blocks, num_splits;
+  int* status;
+};
+
 cudaError_t launch_fwd_f32(const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_fwd_bf16(const FwdParams& p, cudaStream_t stream, const char** why);
 cudaError_t launch_decode_partials(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_split_combine(const CombineParams& p, cudaStream_t stream);
+cudaError_t launch_decode_gather(const GatherParams& p, cudaStream_t stream);
 
 }  // namespace fa
