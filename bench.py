@@ -26,6 +26,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -107,6 +108,25 @@ def traffic_for(kernel_key, src_path):
     return None
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle samples while the timed region runs."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -123,7 +143,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -266,7 +286,7 @@ def run_reference(args, world, rank):
         "data": "synthetic", "config": {"workload": WORKLOAD, "l2": "n/a (CPU)"},
         "decode": {"value": round(gbs, 4), "unit": "GB/s"},
         "cpu_baseline": {"value": round(tf, 6), "unit": "TFLOP/s", "cores": threads,
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": sample, "cpu": cpu_model()},
         "e2e": {"value": round(tf, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -482,7 +502,7 @@ def run_ours(args, world, rank, local):
                             "peak_source": f"{peaks['source']} copy",
                             "bytes_per_launch": int(dec.kv_bytes)},
         "cpu_baseline": {"value": round(tf_cpu, 6), "unit": "TFLOP/s", "cores": threads,
-                         "kind": "oracle",
+                         "kind": "oracle", "cpu": cpu_model(),
                          "sample": f"{rows_cpu} evenly spread query rows of the forward "
                                    f"({dt_cpu:.1f} s)"},
         "e2e": e2e,
@@ -498,7 +518,7 @@ def run_ours(args, world, rank, local):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     args = ap.parse_args(argv)
