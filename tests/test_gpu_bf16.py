@@ -6,6 +6,8 @@ the full-size workloads compare sampled rows that cover every query tile,
 tile boundaries and the causal diagonal, in the launch configuration the
 bench times.
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -254,3 +256,27 @@ def test_varlen_result_does_not_depend_on_sequence_order():
     for j, s in enumerate(perm):
         assert np.array_equal(o1h[cu[s]:cu[s + 1]], o2h[cu2[j]:cu2[j + 1]]), f"sequence {s}"
         assert np.array_equal(l1h[:, cu[s]:cu[s + 1]], l2h[:, cu2[j]:cu2[j + 1]]), f"sequence {s}"
+
+
+def test_varlen_sequence_with_65535_key_tiles_is_scheduled():
+    """The sorted schedule's per-combination work count is 16 bits wide: one
+    query row against 65535 * 128 keys makes 1 + 65535 tile steps, which must
+    saturate rather than wrap to 0 (a combination with 0 work is skipped).
+    Closed form: Q = 0 gives every key the same score, so O is the mean of V
+    and LSE = ln m; V row t is (t mod 8) / 8 in every column, whose mean over
+    whole periods is 7/16, and every partial sum the kernel forms is an
+    integer multiple of 1/8 below 2^22, so the result is exact."""
+    m = 65535 * 128
+    d = 64
+    q = torch.zeros((1, 1, d), dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros((m, 1, d), dtype=torch.bfloat16, device="cuda")
+    v = ((torch.arange(m, device="cuda") % 8).to(torch.float32) / 8).to(torch.bfloat16)
+    v = v[:, None, None].expand(m, 1, d).contiguous()
+    o = torch.zeros((1, 1, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((1, 1), dtype=torch.float32, device="cuda")
+    cu_q = dev_i32([0, 1])
+    cu_k = dev_i32([0, m])
+    fb.fa_forward_varlen(q, k, v, o, lse, cu_q, cu_k, 1, 1, m, 1, m, 1, 1, d, d, d ** -0.5, 0)
+    assert fb.fa_get_device_status() == 0
+    assert torch.all(o.float() == 0.4375), o.float().unique()
+    assert abs(float(lse[0, 0]) - math.log(m)) < 1e-5

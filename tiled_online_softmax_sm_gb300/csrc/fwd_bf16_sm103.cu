@@ -265,8 +265,9 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     for (int c = threadIdx.x; c < C; c += blockDim.x) {
       const Unit U = unit_bt(c / num_pairs, 0, c % num_pairs);
       if (U.bad) atomicExch(status, kDevInvalidArg);  // skipped, touches nothing
-      // a unit with query rows but no keys still writes O = 0 and LSE = -inf
-      sh.work[c] = (uint16_t)(U.rows ? 1 + U.n_kv[0] + U.n_kv[1] : 0);
+      // a unit with query rows but no keys still writes O = 0 and LSE = -inf;
+      // the count saturates (a 16-bit wrap could reach 0 and drop the unit)
+      sh.work[c] = (uint16_t)(U.rows ? min(1 + U.n_kv[0] + U.n_kv[1], 65535) : 0);
     }
     __syncthreads();
     int mine = 0;
