@@ -69,7 +69,8 @@ typedef enum {
  *   scale  multiplies Q K^T; must be positive and finite (pass 1/sqrt(d)
  *          for the usual attention)
  *   causal 0 or 1
- * Supported: d == dv, d in {64, 128}; pointers 16-byte aligned; n, m >= 0.
+ * Supported: d == dv, d in {64, 128}; pointers 16-byte aligned; n, m >= 0;
+ * B*n, B*m and H*n below 2^31 (token rows and the LSE stride are 32-bit).
  * Computes S = Q K^T and P V on the tcgen05 tensor cores (bf16 operands,
  * fp32 accumulation in tensor memory); P is rounded to bf16 before P V.
  */
@@ -88,7 +89,7 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
  * in [0, 256] under the lazy rescale, inside e4m3's range) before P V.
  *   q, k, v   e4m3 bytes [B][n][H][d], [B][m][Hkv][d], [B][m][Hkv][dv]
  *   descales  positive finite fp32
- * Supported: d == dv == 128.
+ * Supported: d == dv == 128; B*n, B*m and H*n below 2^31.
  */
 fa_status fa_forward_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
                          int B, int H, int Hkv, int n, int m, int d, int dv, float scale,
@@ -101,7 +102,7 @@ fa_status fa_forward_fp8(const void* q, const void* k, const void* v, void* o, f
  * IEEE fp32 on the CUDA cores (no TF32); each score is carried as a
  * compensated (hi, lo) pair so that exp(s - m) keeps fp32 relative accuracy
  * when the scores are in the hundreds.
- * Supported: d, dv in {64, 128}; pointers 16-byte aligned.
+ * Supported: d, dv in {64, 128}; pointers 16-byte aligned; H, B <= 65535.
  */
 fa_status fa_forward_f32(const float* q, const float* k, const float* v, float* o, float* lse,
                          int B, int H, int Hkv, int n, int m, int d, int dv,

@@ -57,6 +57,23 @@ def test_forward_validation(lib):
     assert _fwd(lib, n=0) == fb.FA_OK
 
 
+def test_dense_size_limits(lib):
+    # token rows b*n + i and the LSE stride H*n are 32-bit in the kernels
+    big = 1 << 30
+    assert lib.fa_forward(16, 16, 16, 16, 16, 2, 1, 1, big, 1, 128, 128, 0.1, 0, None) == \
+        fb.FA_ERR_UNSUPPORTED
+    assert lib.fa_forward(16, 16, 16, 16, 16, 1, 2, 2, big, 1, 64, 64, 0.1, 0, None) == \
+        fb.FA_ERR_UNSUPPORTED
+    assert lib.fa_forward(16, 16, 16, 16, 16, 2, 1, 1, 1, big, 128, 128, 0.1, 0, None) == \
+        fb.FA_ERR_UNSUPPORTED
+    assert lib.fa_forward_fp8(16, 16, 16, 16, 16, 2, 1, 1, big, 1, 128, 128, 0.1, 1.0, 1.0, 1.0,
+                              0, None) == fb.FA_ERR_UNSUPPORTED
+    assert lib.fa_forward_f32(16, 16, 16, 16, 16, 1, 65536, 1, 8, 8, 64, 64, 0.1, 0, None) == \
+        fb.FA_ERR_UNSUPPORTED
+    assert lib.fa_forward_f32(16, 16, 16, 16, 16, 65536, 1, 1, 8, 8, 64, 64, 0.1, 0, None) == \
+        fb.FA_ERR_UNSUPPORTED
+
+
 def test_forward_f32_and_varlen_validation(lib):
     assert lib.fa_forward_f32(16, 16, 16, 16, 16, 1, 4, 3, 8, 8, 64, 64, 0.1, 0, None) == fb.FA_ERR_INVALID_ARG
     assert lib.fa_forward_f32(16, 16, 16, 16, 16, 1, 4, 2, 8, 8, 32, 64, 0.1, 0, None) == fb.FA_ERR_UNSUPPORTED

@@ -70,6 +70,15 @@ fa_status check_dense(const void* q, const void* k, const void* v, const void* o
   return FA_OK;
 }
 
+// Dense layouts: the kernels form token rows b*n + i and b*m + j, and the LSE
+// stride H*n, in 32-bit ints.
+fa_status check_rows(int B, int H, int n, int m, const char* fn) {
+  const long long lim = 2147483647LL;
+  if ((long long)B * n > lim || (long long)B * m > lim || (long long)H * n > lim)
+    return fail(FA_ERR_UNSUPPORTED, "%s: B*n, B*m and H*n must stay below 2^31", fn);
+  return FA_OK;
+}
+
 }  // namespace
 
 // Shared with the other C-ABI translation units (same error text and status word).
@@ -109,6 +118,7 @@ fa_status fa_forward(const void* q, const void* k, const void* v, void* o, float
   if (!(d == dv && (d == 64 || d == 128)))
     return fail(FA_ERR_UNSUPPORTED, "fa_forward: d=%d dv=%d (supported: d == dv in {64, 128})", d,
                 dv);
+  if ((st = check_rows(B, H, n, m, "fa_forward")) != FA_OK) return st;
   if (B == 0 || n == 0) return FA_OK;
   int* sp = nullptr;
   if ((st = status_ptr(&sp)) != FA_OK) return st;
@@ -133,6 +143,7 @@ fa_status fa_forward_fp8(const void* q, const void* k, const void* v, void* o, f
     return fail(FA_ERR_INVALID_ARG, "fa_forward_fp8: descale factors must be positive and finite");
   if (!(d == 128 && dv == 128))
     return fail(FA_ERR_UNSUPPORTED, "fa_forward_fp8: d=%d dv=%d (supported: 128)", d, dv);
+  if ((st = check_rows(B, H, n, m, "fa_forward_fp8")) != FA_OK) return st;
   if (B == 0 || n == 0) return FA_OK;
   int* sp = nullptr;
   if ((st = status_ptr(&sp)) != FA_OK) return st;
@@ -155,6 +166,9 @@ fa_status fa_forward_f32(const float* q, const float* k, const float* v, float* 
   if (st != FA_OK) return st;
   if (!((d == 64 || d == 128) && (dv == 64 || dv == 128)))
     return fail(FA_ERR_UNSUPPORTED, "fa_forward_f32: d=%d dv=%d (supported: 64, 128)", d, dv);
+  // one CTA row block per (query block, head, batch): grid y and z hold H and B
+  if (H > 65535 || B > 65535)
+    return fail(FA_ERR_UNSUPPORTED, "fa_forward_f32: H=%d B=%d (at most 65535 each)", H, B);
   if (B == 0 || n == 0) return FA_OK;
   int* sp = nullptr;
   if ((st = status_ptr(&sp)) != FA_OK) return st;
