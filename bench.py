@@ -17,7 +17,11 @@ two forwards.
 --impl reference times the float64 CPU oracle on the host cores on a bounded
 sample of the same workload (the only other code this file may run).
 Under torchrun each rank runs the same per-GPU workload (weak scaling, no
-collective on the data path); rank 0 prints the JSON line.
+collective on the data path); rank 0 prints the JSON line.  At N=1 the line
+also carries "configs": every workload of the path timed on the GPU (median
+of 20 launches, as tiled_online_softmax_sm_gb300.timing reports them) beside
+the oracle's rate on a bounded sample of the same inputs (--no-configs skips
+it).
 """
 from __future__ import annotations
 
@@ -247,6 +251,60 @@ def cpu_oracle_decode_sample(case, target_s: float = 4.0):
     return nbytes / dt / 1e9, dt, len(sel)
 
 
+def cpu_oracle_varlen_sample(case, target_s: float = 2.0):
+    """Time the oracle's packed ragged attention on whole sequences, taken in
+    index order and doubling in number until a run takes about target_s;
+    returns (TFLOP/s, seconds, sequences)."""
+    import oracle
+    S = len(case.lens)
+    take = 1
+    while True:
+        L = case.lens[:take]
+        T = int(np.sum(L))
+        cu = np.concatenate([[0], np.cumsum(L)]).astype(np.int32)
+        t = time.perf_counter()
+        oracle.varlen(case.q.values[:T], case.k.values[:T], case.v.values[:T], cu, cu, case.scale,
+                      True)
+        dt = time.perf_counter() - t
+        if dt * 2 > target_s or take >= S:
+            break
+        take = min(S, take * 2)
+    d, dv, H = case.q.values.shape[2], case.v.values.shape[2], case.q.values.shape[1]
+    flops = sum(2.0 * int(x) * (int(x) + 1) * (d + dv) * H / 2 for x in L)
+    return flops / dt / 1e12, dt, take
+
+
+def config_table():
+    """Every workload of the path on the GPU (median of 20 launches each, as
+    the timing tool reports them) beside the float64 oracle timed on a
+    bounded sample of the same inputs on the host cores."""
+    import oracle
+    from tiled_online_softmax_sm_gb300 import inputs as I
+    from tiled_online_softmax_sm_gb300 import timing
+    table = {name: {"gpu": {"ms": round(ms, 4), "rate": round(rate, 2), "unit": unit}}
+             for name, ms, rate, unit in timing.rows(20, 5)}
+    c1 = I.c1_fp32()
+    t = time.perf_counter()
+    oracle.attention(c1.q.values, c1.k.values, c1.v.values, c1.scale, False)
+    dt = time.perf_counter() - t
+    table["fp32 n=m=256 d=64 (graph replay)"]["oracle"] = {
+        "rate": round(4.0 * 256 * 256 * 64 / dt / 1e12, 6), "unit": "TFLOP/s",
+        "seconds": round(dt, 4), "sample": "the whole problem"}
+    for causal in (False, True):
+        c2 = I.c2_bf16(causal=causal)
+        tf, dt, rows, _ = cpu_oracle_forward_sample(c2, target_s=2.0)
+        table[f"bf16 B=4 H=16 n=m=2048 d=128 causal={causal}"]["oracle"] = {
+            "rate": round(tf, 6), "unit": "TFLOP/s", "seconds": round(dt, 3),
+            "sample": f"{rows} of {4 * 16 * 2048} query rows, evenly spread"}
+    for d in (64, 128):
+        c5 = I.c5_varlen(d)
+        tf, dt, seqs = cpu_oracle_varlen_sample(c5, target_s=2.0)
+        table[f"ragged causal varlen 16 seqs H=16 d={d}"]["oracle"] = {
+            "rate": round(tf, 6), "unit": "TFLOP/s", "seconds": round(dt, 3),
+            "sample": f"the first {seqs} of 16 sequences, all rows"}
+    return table
+
+
 # --------------------------------------------------------------- main arms
 def build_inputs(rank: int, world: int = 1):
     """This rank's share of the global job: the job is `world` independent
@@ -472,6 +530,18 @@ def run_ours(args, world, rank, local):
     # CPU baseline: the float64 oracle on a bounded sample of the forward
     tf_cpu, dt_cpu, rows_cpu, threads = cpu_oracle_forward_sample(fwd, target_s=8.0)
 
+    # every workload of the path, GPU and oracle side by side (after the timed
+    # region, one GPU only)
+    configs = None
+    if world == 1 and args.configs:
+        configs = config_table()
+        gbs, ddt, seqs = cpu_oracle_decode_sample(dec, target_s=2.0)
+        for name in configs:
+            if name.startswith("paged decode"):
+                configs[name]["oracle"] = {"rate": round(gbs, 4), "unit": "GB/s",
+                                           "seconds": round(ddt, 3),
+                                           "sample": f"{seqs} of 64 sequences, unsplit"}
+
     line = {
         "metric": METRIC,
         "value": round(fwd_tflops, 3),
@@ -509,6 +579,8 @@ def run_ours(args, world, rank, local):
         "gpu_launches": 3 * K,
         "clocks": clocks,
     }
+    if configs is not None:
+        line["configs"] = configs
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -521,6 +593,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-configs", dest="configs", action="store_false",
+                    help="skip the per-workload GPU and oracle table (N=1 only)")
     args = ap.parse_args(argv)
     world, rank, local = dist_info()
     if args.impl == "reference":
