@@ -45,8 +45,9 @@ sys.path.insert(0, ROOT)
 METRIC = "attn fwd TFLOP/s & % bf16 tensor peak; paged decode HBM GB/s & % peak"
 FWD_SHAPE = dict(B=1, H=32, n=8192, m=8192, d=128, causal=True)
 DECODE_SPLITS = 8
-WORKLOAD = ("long-context causal prefill bf16 B=1 H=32 n=m=8192 d=dv=128 + paged GQA decode "
-            "bf16 64 seqs H=32 Hkv=8 d=128 page 16 ctx U[512,8192] split 8")
+def workload_name(splits: int) -> str:
+    return ("long-context causal prefill bf16 B=1 H=32 n=m=8192 d=dv=128 + paged GQA decode "
+            f"bf16 64 seqs H=32 Hkv=8 d=128 page 16 ctx U[512,8192] split {splits}")
 FWD_KERNEL_SRC = os.path.join(ROOT, "tiled_online_softmax_sm_gb300", "csrc", "fwd_bf16_sm103.cu")
 DEC_KERNEL_SRC = os.path.join(ROOT, "tiled_online_softmax_sm_gb300", "csrc", "decode.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
@@ -274,14 +275,26 @@ def cpu_oracle_varlen_sample(case, target_s: float = 2.0):
     return flops / dt / 1e12, dt, take
 
 
-def config_table():
+def config_table(peaks):
     """Every workload of the path on the GPU (median of 20 launches each, as
-    the timing tool reports them) beside the float64 oracle timed on a
-    bounded sample of the same inputs on the host cores."""
+    the timing tool reports them, with the fraction of the measured peak that
+    bounds it) beside the float64 oracle timed on a bounded sample of the
+    same inputs on the host cores."""
     import oracle
     from tiled_online_softmax_sm_gb300 import inputs as I
     from tiled_online_softmax_sm_gb300 import timing
-    table = {name: {"gpu": {"ms": round(ms, 4), "rate": round(rate, 2), "unit": unit}}
+
+    def frac(name, rate, unit):
+        if name.startswith("fp32"):
+            return None   # a few microseconds: bound by latency, not by a pipe
+        if unit == "GB/s":
+            return round(rate / peaks["hbm_gbs"], 4)
+        # e4m3 runs at twice the bf16 tensor rate (nominal 4.5 vs 2.25 PFLOP/s)
+        peak = peaks["bf16_tflops"] * (2.0 if name.startswith("e4m3") else 1.0)
+        return round(rate / peak, 4)
+
+    table = {name: {"gpu": {"ms": round(ms, 4), "rate": round(rate, 2), "unit": unit,
+                            "frac": frac(name, rate, unit)}}
              for name, ms, rate, unit in timing.rows(20, 5)}
     c1 = I.c1_fp32()
     t = time.perf_counter()
@@ -306,16 +319,17 @@ def config_table():
 
 
 # --------------------------------------------------------------- main arms
-def build_inputs(rank: int, world: int = 1):
+def build_inputs(rank: int, world: int = 1, seed: int | None = None):
     """This rank's share of the global job: the job is `world` independent
     copies of the per-GPU workload (forward batch + decode batch), each with
-    its own seed; rank r takes copy r (weak scaling)."""
+    its own seed (seed + copy); rank r takes copy r (weak scaling)."""
     from tiled_online_softmax_sm_gb300 import inputs as I
     (copy,) = shard_units(world, rank, world)
-    fwd = I.dense_case(I.BASE_SEED + copy, FWD_SHAPE["B"], FWD_SHAPE["H"], FWD_SHAPE["n"],
+    seed = I.BASE_SEED if seed is None else seed
+    fwd = I.dense_case(seed + copy, FWD_SHAPE["B"], FWD_SHAPE["H"], FWD_SHAPE["n"],
                        FWD_SHAPE["m"], FWD_SHAPE["d"], dtype="bf16", causal=True, stream=3,
                        name="c3")
-    dec = I.c4_decode(seed=I.BASE_SEED + copy)
+    dec = I.c4_decode(seed=seed + copy)
     return fwd, dec
 
 
@@ -323,7 +337,7 @@ def run_reference(args, world, rank):
     """The float64 CPU oracle, timed on the host cores (rank 0 only)."""
     if rank != 0:
         return 0
-    fwd, dec = build_inputs(0)
+    fwd, dec = build_inputs(0, 1, args.seed)
     # one sample size for every step: the whole run stays within a few minutes
     per_step_s = min(8.0, max(0.05, 150.0 / max(1, args.steps + args.warmup)))
     _, _, count, threads = cpu_oracle_forward_sample(fwd, target_s=per_step_s)
@@ -341,7 +355,8 @@ def run_reference(args, world, rank):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1000 * statistics.median(x[1] for x in steps), 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": WORKLOAD, "l2": "n/a (CPU)"},
+        "data": "synthetic",
+        "config": {"workload": workload_name(args.splits), "l2": "n/a (CPU)"},
         "decode": {"value": round(gbs, 4), "unit": "GB/s"},
         "cpu_baseline": {"value": round(tf, 6), "unit": "TFLOP/s", "cores": threads,
                          "kind": "oracle", "sample": sample, "cpu": cpu_model()},
@@ -363,7 +378,7 @@ def run_ours(args, world, rank, local):
         dist.init_process_group("nccl", device_id=dev)
     fb.load()
 
-    fwd, dec = build_inputs(rank, world)
+    fwd, dec = build_inputs(rank, world, args.seed)
 
     def to_dev(t):
         return torch.from_numpy(t.data.view(np.int16)).to(dev).view(torch.bfloat16)
@@ -376,7 +391,7 @@ def run_ours(args, world, rank, local):
     dbt = torch.from_numpy(dec.block_table).to(dev)
     dsl = torch.from_numpy(dec.seq_lens).to(dev)
     S = len(dec.seq_lens)
-    ws_bytes = fb.fa_paged_decode_workspace_size(S, dec.H, dec.dv, DECODE_SPLITS)
+    ws_bytes = fb.fa_paged_decode_workspace_size(S, dec.H, dec.dv, args.splits)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     dout = torch.empty((S, dec.H, dec.dv), dtype=torch.bfloat16, device=dev)
     dlse = torch.empty((S, dec.H), dtype=torch.float32, device=dev)
@@ -387,7 +402,7 @@ def run_ours(args, world, rank, local):
 
     def decode():
         fb.fa_paged_decode(dq, dkc, dvc, dbt, dsl, dout, dlse, S, dec.H, dec.Hkv, dec.d, dec.dv,
-                           dec.page_size, dec.num_pages, dec.max_blocks, DECODE_SPLITS, dec.scale,
+                           dec.page_size, dec.num_pages, dec.max_blocks, args.splits, dec.scale,
                            ws, ws_bytes, stream)
 
     warmup = max(3, args.warmup)
@@ -534,7 +549,7 @@ def run_ours(args, world, rank, local):
     # region, one GPU only)
     configs = None
     if world == 1 and args.configs:
-        configs = config_table()
+        configs = config_table(peaks)
         gbs, ddt, seqs = cpu_oracle_decode_sample(dec, target_s=2.0)
         for name in configs:
             if name.startswith("paged decode"):
@@ -555,8 +570,8 @@ def run_ours(args, world, rank, local):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "fwd_ms": round(fwd_avg, 4), "decode_ms": round(dec_avg, 4),
-                   "decode_splits": DECODE_SPLITS,
+        "config": {"workload": workload_name(args.splits), "fwd_ms": round(fwd_avg, 4),
+                   "decode_ms": round(dec_avg, 4), "decode_splits": args.splits,
                    "l2": "inputs larger than L2 (forward 192 MB, KV cache 1.3 GB streamed each step)"},
         "decode": {"value": round(dec_gbs, 2), "unit": "GB/s", "kv_bytes": int(dec.kv_bytes),
                    "frac_of_hbm_peak": round(dec_achieved / peaks["hbm_gbs"], 4)},
@@ -593,6 +608,10 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--splits", type=int, default=DECODE_SPLITS,
+                    help="KV splits of the decode step (1..64)")
+    ap.add_argument("--seed", type=int, default=None,
+                    help="base seed of the synthetic inputs (default: the generators' own)")
     ap.add_argument("--no-configs", dest="configs", action="store_false",
                     help="skip the per-workload GPU and oracle table (N=1 only)")
     args = ap.parse_args(argv)
