@@ -156,8 +156,9 @@ fa_status fa_forward_varlen(const void* q, const void* k, const void* v, void* o
  * fa_forward.  Cache contents past seq_lens[s] in the last page are never
  * used, NaN included.  Page ids are range-checked on the device (an id
  * outside [0, num_pages) reads page 0 and sets FA_ERR_BAD_BLOCK_TABLE);
- * sequences whose query offsets fall outside total_q, or whose seq_lens
- * exceed the table, are skipped and set FA_ERR_INVALID_ARG.
+ * sequences whose query offsets fall outside total_q, or whose seq_lens[s]
+ * falls outside [0, max_blocks_per_seq*page_size], are skipped (none of their
+ * rows is written) and set FA_ERR_INVALID_ARG.
  * Supported: d == dv in {64, 128}, page_size == 16.
  */
 fa_status fa_paged_prefill(const void* q, const void* k_cache, const void* v_cache,
