@@ -52,7 +52,10 @@ typedef enum {
     FA_ERR_WORKSPACE = 3,     /* workspace pointer null or smaller than the size query returns */
     FA_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed; fa_last_error() has the text */
     FA_ERR_TIMEOUT = 5,       /* device status: a pipeline wait exceeded its limit */
-    FA_ERR_BAD_BLOCK_TABLE = 6 /* device status: a block-table id outside [0, num_pages) */
+    FA_ERR_BAD_BLOCK_TABLE = 6, /* device status: a block-table id outside [0, num_pages) */
+    FA_ERR_DEBUG_CHECK = 7    /* device status, debug build (libfa_gb300_debug.so) only: a
+                                 kernel's output index left the buffer it was given; the store
+                                 was skipped.  Never set by the normal build. */
 } fa_status;
 
 /*

@@ -18,7 +18,9 @@ import os
 import threading
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libfa_gb300.so")
+# FA_LIBRARY selects another build of the same ABI (the debug build,
+# libfa_gb300_debug.so, for instance); by default the in-tree library.
+LIB_PATH = os.environ.get("FA_LIBRARY") or os.path.join(HERE, "libfa_gb300.so")
 
 FA_OK = 0
 FA_ERR_INVALID_ARG = 1
@@ -27,6 +29,7 @@ FA_ERR_WORKSPACE = 3
 FA_ERR_CUDA = 4
 FA_ERR_TIMEOUT = 5
 FA_ERR_BAD_BLOCK_TABLE = 6
+FA_ERR_DEBUG_CHECK = 7
 
 EXPORTED = ("fa_forward", "fa_forward_fp8", "fa_forward_f32", "fa_forward_varlen", "fa_paged_prefill",
             "fa_paged_decode_workspace_size",

@@ -318,6 +318,7 @@ decode_partials_kernel(const __grid_constant__ CUtensorMap tmK,
     const int r = r0 + hr * 8;
     if (r >= G) continue;
     const size_t idx = ((size_t)s * H + g * G + r) * X + x;
+    if (!FA_IN_BOUNDS(idx, (size_t)num_seqs * H * X, status)) continue;
     if ((lane & 3) == 0) {
       part_m[idx] = m_run[hr] == -INFINITY ? -INFINITY : m_run[hr] * kLn2;
       part_l[idx] = l_run[hr];
@@ -456,7 +457,9 @@ decode_gather_kernel(const __grid_constant__ CUtensorMap tmK,
       const uint4 val = *reinterpret_cast<const uint4*>(stage + which * kPageBytes +
                                                         (u >> 3) * kHalfBytes + swz(row, u & 7));
       __nv_bfloat16* out = which ? v_out : k_out;
-      *reinterpret_cast<uint4*>(out + ((row0 + (size_t)p * kPage + row) * Hkv + g) * kD + u * 8) = val;
+      const size_t orow = (row0 + (size_t)p * kPage + row) * Hkv + g;
+      if (FA_IN_BOUNDS(orow, (size_t)num_seqs * max_blocks * kPage * Hkv, status))
+        *reinterpret_cast<uint4*>(out + orow * kD + u * 8) = val;
     }
     __syncwarp();
   }

@@ -9,7 +9,26 @@
 namespace fa {
 
 // Device status codes written by kernels (same values as fa_status).
-enum : int { kDevOk = 0, kDevInvalidArg = 1, kDevTimeout = 5, kDevBadBlockTable = 6 };
+enum : int {
+  kDevOk = 0,
+  kDevInvalidArg = 1,
+  kDevTimeout = 5,
+  kDevBadBlockTable = 6,
+  kDevDebugCheck = 7
+};
+
+// Debug builds (-DFA_DEBUG: libfa_gb300_debug.so) check each global store's
+// index against the size of the buffer the kernel was given; a failed check
+// records kDevDebugCheck in the status word and the store is skipped instead
+// of landing outside the buffer.  In the normal build the check is the
+// constant true and neither operand is evaluated.
+#ifdef FA_DEBUG
+#define FA_IN_BOUNDS(idx, limit, status)                     \
+  (((size_t)(idx) < (size_t)(limit)) ? true                  \
+                                     : (atomicExch((status), kDevDebugCheck), false))
+#else
+#define FA_IN_BOUNDS(idx, limit, status) true
+#endif
 
 // Forward problem.  Dense BSHD when cu_q == nullptr; otherwise packed varlen
 // (B = number of sequences, n/m = max lengths, token rows start at cu_q[b]).

@@ -699,7 +699,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
           for (int e = 0; e < 32; ++e) ov[c][e] = 0u;
       }
-      if (row_valid) {
+      // O has total_q * H rows of D (dense: total_q = B * n); LSE as many entries
+      if (row_valid && FA_IN_BOUNDS(orow, (size_t)total_q * H, status)) {
         const float inv = l_run > 0.f ? out_scale / l_run : 0.f;
         uint4* dst = reinterpret_cast<uint4*>(o + orow * D);
 #pragma unroll
@@ -713,10 +714,10 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             v.w = ptx::pack_bf16x2(__uint_as_float(ov[c][8 * w + 6]) * inv, __uint_as_float(ov[c][8 * w + 7]) * inv);
             dst[c * 4 + w] = v;
           }
-        if (lse != nullptr)
-          lse[(size_t)U.b * lse_stride_b + (size_t)U.h * lse_stride_h +
-              (U.q_row0 - (cu_q ? 0 : U.b * n)) + qi] =
-              l_run > 0.f ? (m_ref + __log2f(l_run)) * kLn2 : -INFINITY;
+        const size_t li = (size_t)U.b * lse_stride_b + (size_t)U.h * lse_stride_h +
+                          (U.q_row0 - (cu_q ? 0 : U.b * n)) + qi;
+        if (lse != nullptr && FA_IN_BOUNDS(li, (size_t)total_q * H, status))
+          lse[li] = l_run > 0.f ? (m_ref + __log2f(l_run)) * kLn2 : -INFINITY;
       }
     }
   }

@@ -80,7 +80,7 @@ template <int D, int DV>
 __global__ void __launch_bounds__(kThreads)
 fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
                const float* __restrict__ v, float* __restrict__ o, float* __restrict__ lse,
-               int B, int H, int Hkv, int n, int m, float scale, int causal) {
+               int B, int H, int Hkv, int n, int m, float scale, int causal, int* status) {
   extern __shared__ float4 smem4[];
   const int group = threadIdx.x / kGroupThreads;
   const int tid = threadIdx.x % kGroupThreads;   // thread within its group
@@ -251,8 +251,10 @@ fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
   m_lo = g_lo;
 
   if (!row_valid) return;
+  const size_t oi = ((size_t)b * n + i) * H + h;   // O has B * n * H rows of DV
+  if (!FA_IN_BOUNDS(oi, (size_t)B * n * H, status)) return;
   const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-  float4* orow = reinterpret_cast<float4*>(o + (((size_t)b * n + i) * H + h) * DV);
+  float4* orow = reinterpret_cast<float4*>(o + oi * DV);
 #pragma unroll
   for (int c = 0; c < VC; ++c) {
     const float4 x = acc[c];
@@ -275,7 +277,7 @@ cudaError_t launch(const FwdParams& p, cudaStream_t stream) {
   fwd_f32_kernel<D, DV><<<grid, kThreads, smem, stream>>>(
       static_cast<const float*>(p.q), static_cast<const float*>(p.k),
       static_cast<const float*>(p.v), static_cast<float*>(p.o), p.lse, p.B, p.H, p.Hkv, p.n,
-      p.m, p.scale, p.causal);
+      p.m, p.scale, p.causal, p.status);
   return cudaGetLastError();
 }
 
