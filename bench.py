@@ -602,7 +602,7 @@ def run_ours(args, world, rank, local):
     return 0
 
 
-def main(argv=None):
+def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
@@ -615,6 +615,15 @@ def main(argv=None):
     ap.add_argument("--no-configs", dest="configs", action="store_false",
                     help="skip the per-workload GPU and oracle table (N=1 only)")
     args = ap.parse_args(argv)
+    if not 1 <= args.splits <= 64:
+        ap.error(f"--splits {args.splits}: the decode takes 1..64 splits")
+    if args.steps < 1 or args.warmup < 0:
+        ap.error("--steps must be >= 1 and --warmup >= 0")
+    return args
+
+
+def main(argv=None):
+    args = parse_args(argv)
     world, rank, local = dist_info()
     if args.impl == "reference":
         return run_reference(args, world, rank)
