@@ -7,6 +7,7 @@ Workloads (sizes as in the bench and the parity tests):
   fwd_c2     non-causal bf16 forward, B=4 H=16 n=m=2048 d=128
   fwd_c2c    causal bf16 forward, B=4 H=16 n=m=2048 d=128
   varlen_c5  ragged causal bf16 varlen forward, 16 sequences, d=128
+  varlen_c5_d64  the same at d=64
   decode_c4  paged grouped-head decode, 64 sequences, H=32 Hkv=8, 8 splits (1.3 GB KV)
   fp8_c3     causal e4m3 forward, B=1 H=32 n=m=8192 d=128
   prefill_c4 paged prefill: 512-token chunks of 16 sequences of the decode pool
@@ -39,8 +40,8 @@ def make(name: str, splits: int = 8):
         lse = torch.empty((c.B, c.H, c.n), dtype=torch.float32, device="cuda")
         return lambda: fb.fa_forward(q, k, v, o, lse, c.B, c.H, c.Hkv, c.n, c.m, c.d, c.dv,
                                      c.scale, int(c.causal))
-    if name == "varlen_c5":
-        c = I.c5_varlen(128)
+    if name in ("varlen_c5", "varlen_c5_d64"):
+        c = I.c5_varlen(64 if name.endswith("d64") else 128)
         q, k, v = _dev(c.q), _dev(c.k), _dev(c.v)
         cu = torch.from_numpy(c.cu_seqlens).cuda()
         T = int(c.cu_seqlens[-1])
