@@ -19,7 +19,8 @@ def lib():
 
 
 def _declared():
-    src = open(os.path.join(ROOT, "include", "fa.h")).read()
+    with open(os.path.join(ROOT, "include", "fa.h")) as f:
+        src = f.read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", src)))
 
