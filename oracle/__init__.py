@@ -58,11 +58,12 @@ def _load():
             lib.oracle_decode_partials_f64.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, D, P, P, P]
             lib.oracle_split_combine_f64.argtypes = [P, P, P, I, I, I, I, P, P]
             lib.oracle_online_recurrence_f64.argtypes = [P, P, P, I, I, I, I, D, I, I, I, P, P, P]
+            lib.oracle_set_num_threads.argtypes = [I]
             for f in ("oracle_attention_rows_f64", "oracle_attention_f64", "oracle_varlen_f64",
                       "oracle_paged_decode_f64", "oracle_paged_prefill_f64",
                       "oracle_decode_partials_f64",
                       "oracle_split_combine_f64", "oracle_online_recurrence_f64",
-                      "oracle_num_threads"):
+                      "oracle_num_threads", "oracle_set_num_threads"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -93,6 +94,12 @@ def _check(rc, what):
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> int:
+    """Threads the following oracle calls use; returns the previous count.
+    Results do not depend on it (each row is one thread's loop)."""
+    return int(_load().oracle_set_num_threads(int(n)))
 
 
 def attention(q, k, v, scale, causal=False):

@@ -601,3 +601,15 @@ int oracle_num_threads(void)
     return 1;
 #endif
 }
+
+/* Threads the following calls use (for timing the oracle on one core and on
+ * all of them); returns the previous count.  The results do not depend on it:
+ * every row is computed by one thread in the same order. */
+int oracle_set_num_threads(int n)
+{
+    const int prev = oracle_num_threads();
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#endif
+    return prev;
+}

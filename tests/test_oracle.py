@@ -470,3 +470,18 @@ def test_pins_discriminate_plausible_slips():
     o, lse = oracle.attention(q, k, v, scale, True)
     np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12)
     np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-12)
+
+
+def test_results_do_not_depend_on_the_thread_count():
+    """The oracle's rows are each one thread's loop, so one thread and all of
+    them give the same bits (the bench times it both ways)."""
+    c = I.dense_case(12, 2, 3, 70, 90, 64, Hkv=1, causal=True)
+    o_all, lse_all = oracle.attention(c.q.values, c.k.values, c.v.values, c.scale, True)
+    prev = oracle.set_num_threads(1)
+    try:
+        assert oracle.num_threads() == 1
+        o_one, lse_one = oracle.attention(c.q.values, c.k.values, c.v.values, c.scale, True)
+    finally:
+        oracle.set_num_threads(prev)
+    assert oracle.num_threads() == prev
+    assert np.array_equal(o_all, o_one) and np.array_equal(lse_all, lse_one)
