@@ -72,6 +72,10 @@ typedef enum {
  *   scale  multiplies Q K^T; must be positive and finite (pass 1/sqrt(d)
  *          for the usual attention)
  *   causal 0 or 1
+ * Non-finite inputs: the last K/V tile of a batch element may reach into the
+ * next element's rows.  Those keys are masked (their weights are exactly 0),
+ * but 0 * inf is NaN, so an inf or NaN in the next element's V reaches this
+ * element's output too (it already makes that element's own output NaN).
  * Supported: d == dv, d in {64, 128}; pointers 16-byte aligned; n, m >= 0;
  * B*n, B*m and H*n below 2^31 (token rows and the LSE stride are 32-bit).
  * Computes S = Q K^T and P V on the tcgen05 tensor cores (bf16 operands,
@@ -128,6 +132,9 @@ fa_status fa_forward_f32(const float* q, const float* k, const float* v, float* 
  *   max_seqlen_q, max_seqlen_k  upper bounds of the per-sequence lengths
  *        (sizes the launch grid; a larger value only launches idle blocks)
  * Supported as fa_forward; causal uses each sequence's own q and k lengths.
+ * Non-finite V rows of one sequence can reach the previous sequence's output
+ * as in fa_forward.  (The paged paths zero the V rows past a sequence's end,
+ * since a cache page may hold anything there.)
  */
 fa_status fa_forward_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
                             const int* cu_seqlens_q, const int* cu_seqlens_k, int num_seqs,
