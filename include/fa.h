@@ -210,7 +210,8 @@ size_t fa_paged_decode_workspace_size(int num_seqs, int H, int dv, int num_split
  * an id outside [0, num_pages) is skipped and sets FA_ERR_BAD_BLOCK_TABLE.  A
  * seq_lens[s] outside [0, max_blocks_per_seq*page_size] is treated as an
  * empty sequence (O = 0, LSE = -inf) and sets FA_ERR_INVALID_ARG.
- * Supported: d == dv == 128, page_size == 16, H / Hkv <= 16.
+ * Supported: d == dv == 128, page_size == 16, H / Hkv <= 16; num_pages*Hkv*16
+ * and num_seqs*H*num_splits below 2^31.
  */
 fa_status fa_paged_decode(const void* q, const void* k_cache, const void* v_cache,
                           const int* block_table, const int* seq_lens, void* o, float* lse,
@@ -266,7 +267,8 @@ fa_status fa_paged_decode_noalloc(const void* q, const void* k_cache, const void
  *                s*max_blocks_per_seq*page_size + t for t < seq_lens[s]; other
  *                rows are not written.
  * Device status as fa_paged_decode (bad page ids, out-of-range seq_lens).
- * Supported: d == 128, page_size == 16.
+ * Supported: d == 128, page_size == 16; num_pages*Hkv*16 and
+ * num_seqs*Hkv*num_splits below 2^31.
  */
 fa_status fa_paged_gather(const void* k_cache, const void* v_cache, const int* block_table,
                           const int* seq_lens, void* k_out, void* v_out, int num_seqs, int Hkv,
@@ -285,7 +287,7 @@ fa_status fa_paged_gather(const void* k_cache, const void* v_cache, const int* b
  *   o               bf16 [num_seqs][H][dv] written
  *   lse             fp32 [num_seqs][H] written (may be NULL)
  * An (s, h) whose splits are all empty gets O = 0 and LSE = -inf.
- * Supported: dv % 4 == 0, dv <= 256, 1 <= num_splits <= 64.
+ * Supported: dv % 4 == 0, dv <= 256, 1 <= num_splits <= 64; num_seqs*H below 2^31.
  */
 fa_status fa_split_combine(const float* part_m, const float* part_l, const float* part_o,
                            void* o, float* lse, int num_seqs, int H, int num_splits, int dv,

@@ -118,6 +118,9 @@ def test_decode_validation(lib):
     assert _dec(lib, ws=272) == fb.FA_ERR_WORKSPACE            # not 256-byte aligned
     assert _dec(lib, bt=None) == fb.FA_ERR_INVALID_ARG
     assert _dec(lib, S=0) == fb.FA_OK
+    # 32-bit page rows and unit counts
+    assert _dec(lib, P=1 << 25) == fb.FA_ERR_UNSUPPORTED
+    assert _dec(lib, S=1 << 26, X=64) == fb.FA_ERR_UNSUPPORTED
 
 
 def _gather(lib, **kw):
@@ -139,6 +142,8 @@ def test_gather_validation(lib):
     assert _gather(lib, vo=24) == fb.FA_ERR_INVALID_ARG          # not 16-byte aligned
     assert _gather(lib, P=0) == fb.FA_ERR_INVALID_ARG
     assert _gather(lib, S=0) == fb.FA_OK
+    assert _gather(lib, P=1 << 25) == fb.FA_ERR_UNSUPPORTED
+    assert _gather(lib, S=1 << 26, X=64) == fb.FA_ERR_UNSUPPORTED
 
 
 def test_combine_validation(lib):
@@ -146,6 +151,8 @@ def test_combine_validation(lib):
     assert lib.fa_split_combine(16, 16, 16, 16, 16, 4, 8, 4, 130, None) == fb.FA_ERR_UNSUPPORTED
     assert lib.fa_split_combine(None, 16, 16, 16, 16, 4, 8, 4, 128, None) == fb.FA_ERR_INVALID_ARG
     assert lib.fa_split_combine(16, 16, 16, 16, 16, 0, 8, 4, 128, None) == fb.FA_OK
+    assert lib.fa_split_combine(16, 16, 16, 16, 16, 1 << 27, 32, 4, 128, None) == \
+        fb.FA_ERR_UNSUPPORTED
 
 
 def test_missing_library_fails_loudly(tmp_path):

@@ -281,6 +281,10 @@ fa_status fa_paged_decode(const void* q, const void* k_cache, const void* v_cach
     return fail(FA_ERR_INVALID_ARG, "%s: null pointer", fn);
   if (num_pages == 0 || max_blocks_per_seq == 0)
     return fail(FA_ERR_INVALID_ARG, "%s: empty page pool or block table", fn);
+  // page rows (page * Hkv + head) * 16 and the units (sequence, head, split) are 32-bit
+  if ((long long)num_pages * Hkv * 16 > 0x7fffffffLL ||
+      (long long)num_seqs * H * num_splits > 0x7fffffffLL)
+    return fail(FA_ERR_UNSUPPORTED, "%s: page pool or sequences x heads x splits too large", fn);
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(block_table) & 3u) ||
       (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
@@ -328,6 +332,9 @@ fa_status fa_paged_gather(const void* k_cache, const void* v_cache, const int* b
     return fail(FA_ERR_INVALID_ARG, "%s: null pointer", fn);
   if (num_pages == 0 || max_blocks_per_seq == 0)
     return fail(FA_ERR_INVALID_ARG, "%s: empty page pool or block table", fn);
+  if ((long long)num_pages * Hkv * 16 > 0x7fffffffLL ||
+      (long long)num_seqs * Hkv * num_splits > 0x7fffffffLL)
+    return fail(FA_ERR_UNSUPPORTED, "%s: page pool or sequences x heads x splits too large", fn);
   if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_out) || !aligned16(v_out) ||
       (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
     return fail(FA_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
@@ -349,6 +356,8 @@ fa_status fa_split_combine(const float* part_m, const float* part_l, const float
     return fail(FA_ERR_INVALID_ARG, "%s: num_splits=%d outside [1, 64]", fn, num_splits);
   if (dv <= 0 || dv % 4 != 0 || dv > 256)
     return fail(FA_ERR_UNSUPPORTED, "%s: dv=%d (need dv %% 4 == 0, dv <= 256)", fn, dv);
+  if ((long long)num_seqs * H > 0x7fffffffLL)
+    return fail(FA_ERR_UNSUPPORTED, "%s: sequences x heads too large", fn);
   if (num_seqs == 0) return FA_OK;
   if (part_m == nullptr || part_l == nullptr || part_o == nullptr || o == nullptr)
     return fail(FA_ERR_INVALID_ARG, "%s: null pointer", fn);
