@@ -51,3 +51,10 @@ def test_traffic_only_for_the_captured_source(tmp_path, monkeypatch):
 def test_peaks_have_the_roofline_denominators():
     p = bench.measured_peaks()
     assert p["hbm_gbs"] > 0 and p["bf16_tflops"] > 0 and p["source"] in ("measured", "fallback")
+
+
+def test_forward_work_is_the_nominal_halved_count():
+    """4 n m d H B FLOPs, halved when causal: 549.76 GFLOP for the causal
+    B=1 H=32 n=m=8192 d=128 forward the bench times."""
+    assert bench.fwd_flops(**bench.FWD_SHAPE) == 4.0 * 8192 * 8192 * 128 * 32 / 2 == 549755813888.0
+    assert bench.fwd_flops(B=4, H=16, n=2048, m=2048, d=128, causal=False) == 137438953472.0
