@@ -143,6 +143,61 @@ def test_weights_sum_to_one_and_respect_mask():
             np.testing.assert_allclose(o[r], w[r] @ v[b, :, h].astype(np.float64), rtol=0, atol=1e-13)
 
 
+def _row_by_definition(q, k, v, scale, causal, b, h, i, kv_b=None, kv_h=None, q_i=None):
+    """One output row from "手搓 Attention" §2 version 0 with §4's max
+    subtraction, in numpy float64; kv_b, kv_h and q_i override the batch
+    element and kv head whose K/V rows are read and the query row, to play
+    the row-offset slips the selected-rows test must catch."""
+    n, m = q.shape[1], k.shape[1]
+    group = q.shape[2] // k.shape[2]
+    kb = b if kv_b is None else kv_b
+    hk = h // group if kv_h is None else kv_h
+    qi = i if q_i is None else q_i
+    vis = min(m, max(0, i + 1 + (m - n))) if causal else m
+    if vis == 0:
+        return np.zeros(v.shape[-1])
+    s = scale * (k[kb, :vis, hk].astype(np.float64) @ q[b, qi, h].astype(np.float64))
+    w = np.exp(s - s.max())
+    return (w / w.sum()) @ v[kb, :vis, hk].astype(np.float64)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("n, m", [(13, 13), (9, 21), (21, 9)])
+def test_selected_rows_equal_the_full_definition(causal, n, m):
+    """The selected-rows oracle (the checker of the full-size GPU tests and
+    of the CPU baseline) gives, bit for bit, row (b, h, i) of the every-row
+    oracle, which the closed forms above and the library SDPA pin; every
+    (b, h, i) of a batch with B > 1, grouped heads and n != m is asked for,
+    in shuffled order and with repeats ("手搓 Attention" §2 version 0: the
+    definition every other version is checked against).  Row-offset slips
+    (the wrong batch element, kv head or query row), written test-side, each
+    fail the same comparison."""
+    B, H, Hkv, d, dv = 3, 6, 2, 16, 8
+    q = _rand(70, B, n, H, d, scale=2)
+    k = _rand(71, B, m, Hkv, d, scale=2)
+    v = _rand(72, B, m, Hkv, dv)
+    scale = 0.37
+    o, lse = oracle.attention(q, k, v, scale, causal)
+    allrows = np.array([(b, h, i) for b in range(B) for h in range(H) for i in range(n)], np.int32)
+    g = I.rng(73, n, m)
+    rows = np.concatenate([allrows[g.permutation(len(allrows))],
+                           allrows[g.integers(0, len(allrows), size=17)]])
+    o_r, lse_r = oracle.attention_rows(q, k, v, scale, causal, rows)
+    assert np.array_equal(o_r, o[rows[:, 0], rows[:, 2], rows[:, 1]])
+    assert np.array_equal(lse_r, lse[rows[:, 0], rows[:, 1], rows[:, 2]])
+    # the definition written out agrees with both
+    for b, h, i in allrows[:: 7]:
+        want = _row_by_definition(q, k, v, scale, causal, b, h, i)
+        np.testing.assert_allclose(o[b, i, h], want, rtol=0, atol=1e-12)
+    # slips: each reads the wrong rows somewhere and misses by far more than rounding
+    for b, h, i in [(1, 5, n - 1), (2, 2, n - 3), (0, 3, n - 2)]:
+        wrong_b = _row_by_definition(q, k, v, scale, causal, b, h, i, kv_b=(b + 1) % B)
+        wrong_h = _row_by_definition(q, k, v, scale, causal, b, h, i, kv_h=(h // 3 + 1) % Hkv)
+        wrong_i = _row_by_definition(q, k, v, scale, causal, b, h, i, q_i=(i + 1) % n)
+        for bad in (wrong_b, wrong_h, wrong_i):
+            assert np.abs(bad - o[b, i, h]).max() > 1e-3
+
+
 # ----------------------------------------------------------------------------
 # Invariants
 # ----------------------------------------------------------------------------
