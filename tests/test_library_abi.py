@@ -88,6 +88,26 @@ def test_forward_f32_and_varlen_validation(lib):
                                  None) == fb.FA_OK
 
 
+@pytest.mark.parametrize("scale", [0.0, -0.125, float("inf"), float("nan")])
+def test_every_forward_and_decode_refuses_a_scale_that_is_not_positive_and_finite(lib, scale):
+    """Every entry point that takes a softmax scale requires it positive and
+    finite ("手搓 Attention" §1 and §4: the scale is 1/sqrt(d) and the row
+    maximum is taken on scaled scores, which for the fp32 kernel's unscaled
+    maximum only holds for a positive scale)."""
+    assert _fwd(lib, scale=scale) == fb.FA_ERR_INVALID_ARG
+    assert lib.fa_forward_f32(16, 16, 16, 16, 16, 1, 2, 1, 8, 8, 64, 64, scale, 0, None) == \
+        fb.FA_ERR_INVALID_ARG
+    assert lib.fa_forward_fp8(16, 16, 16, 16, 16, 1, 2, 1, 8, 8, 128, 128, scale, 1.0, 1.0, 1.0, 0,
+                              None) == fb.FA_ERR_INVALID_ARG
+    assert lib.fa_forward_varlen(16, 16, 16, 16, 16, 16, 16, 2, 10, 10, 8, 8, 4, 4, 64, 64, scale,
+                                 1, None) == fb.FA_ERR_INVALID_ARG
+    assert lib.fa_paged_prefill(16, 16, 16, 16, 16, 16, 16, 16, 2, 10, 8, 4, 4, 64, 64, 16, 100, 8,
+                                scale, 1, None) == fb.FA_ERR_INVALID_ARG
+    assert _dec(lib, scale=scale) == fb.FA_ERR_INVALID_ARG
+    assert _noalloc(lib, scale=scale) == fb.FA_ERR_INVALID_ARG
+    assert "scale" in fb.fa_last_error()
+
+
 def test_decode_workspace_size(lib):
     S, H, dv, X = 64, 32, 128, 16
     tri = S * H * X
@@ -121,6 +141,29 @@ def test_decode_validation(lib):
     # 32-bit page rows and unit counts
     assert _dec(lib, P=1 << 25) == fb.FA_ERR_UNSUPPORTED
     assert _dec(lib, S=1 << 26, X=64) == fb.FA_ERR_UNSUPPORTED
+
+
+def _noalloc(lib, **kw):
+    a = dict(q=16, kc=16, vc=16, bt=16, sl=16, o=16, lse=16, S=4, H=32, Hkv=8, d=128, dv=128,
+             page=16, P=100, maxb=8, X=4, scale=0.1)
+    a.update(kw)
+    return lib.fa_paged_decode_noalloc(a["q"], a["kc"], a["vc"], a["bt"], a["sl"], a["o"], a["lse"],
+                                       a["S"], a["H"], a["Hkv"], a["d"], a["dv"], a["page"], a["P"],
+                                       a["maxb"], a["X"], a["scale"], None)
+
+
+def test_noalloc_decode_validation(lib):
+    """The allocation-free decode checks its arguments as fa_paged_decode
+    does, before any launch (and before its first-call address lookup)."""
+    assert _noalloc(lib, X=0) == fb.FA_ERR_INVALID_ARG
+    assert _noalloc(lib, H=30) == fb.FA_ERR_INVALID_ARG
+    assert _noalloc(lib, page=32) == fb.FA_ERR_UNSUPPORTED
+    assert _noalloc(lib, d=64, dv=64) == fb.FA_ERR_UNSUPPORTED
+    assert _noalloc(lib, bt=None) == fb.FA_ERR_INVALID_ARG
+    assert _noalloc(lib, q=24) == fb.FA_ERR_INVALID_ARG          # not 16-byte aligned
+    assert _noalloc(lib, S=0) == fb.FA_OK
+    # 32-bit page rows (page * Hkv + head) * 16
+    assert _noalloc(lib, P=1 << 25) == fb.FA_ERR_UNSUPPORTED
 
 
 def _gather(lib, **kw):

@@ -2,9 +2,11 @@
 allocate device memory (plugins whose host framework owns every device
 allocation, serving loops that must not allocate once running).
 
-It must give what fa_paged_decode gives on the same inputs, also on the
-second of two calls in a row (the fixed scratch array keeps the previous
-call's contents), and refuse problems whose partials exceed the array.
+It must give what fa_paged_decode gives on the same inputs, bit for bit (the
+same kernels run on the same inputs; only where the split partials live
+differs), also on the second of two calls in a row (the fixed scratch array
+keeps the previous call's contents); its calls must leave the device's free
+memory unchanged; and it must refuse problems whose partials exceed the array.
 This file is collected last so that a run stopping at the first failure has
 already run every other test; it also passes when run on its own.
 """
@@ -16,7 +18,7 @@ from tiled_online_softmax_sm_gb300 import binding as fb
 from tiled_online_softmax_sm_gb300 import build as fbuild
 from tiled_online_softmax_sm_gb300 import inputs as I
 
-from _helpers import BF16_MAX_ABS, BF16_MEAN_ABS, assert_close, assert_lse_close, dev, dev_i32, host
+from _helpers import dev, dev_i32
 
 
 def _args(case):
@@ -34,6 +36,10 @@ def _noalloc(case, splits, tensors):
     return o, lse
 
 
+def _bits(x):
+    return x.view(torch.int16 if x.dtype == torch.bfloat16 else torch.int32).cpu().numpy()
+
+
 @pytest.mark.gpu
 def test_noalloc_matches_workspace_entry_point_two_calls_in_a_row():
     # first call: many splits; second call: a different problem with fewer,
@@ -48,9 +54,33 @@ def test_noalloc_matches_workspace_entry_point_two_calls_in_a_row():
         o_ref, lse_ref = fb.paged_decode(*t, splits, case.scale)
         o, lse = _noalloc(case, splits, t)
         torch.cuda.synchronize()
-        assert_close(host(o), host(o_ref), BF16_MAX_ABS, BF16_MEAN_ABS, what=f"noalloc X={splits}")
-        assert_lse_close(host(lse), host(lse_ref), what=f"noalloc lse X={splits}")
+        assert np.array_equal(_bits(o), _bits(o_ref)), f"O bits differ at X={splits}"
+        assert np.array_equal(_bits(lse), _bits(lse_ref)), f"LSE bits differ at X={splits}"
         assert fb.fa_get_device_status() == 0
+
+
+@pytest.mark.gpu
+def test_noalloc_calls_leave_free_device_memory_unchanged():
+    """After a first call (which only looks up the array's address), further
+    calls take no device memory: the free bytes the driver reports do not move."""
+    case = I.decode_case(73, num_seqs=8, H=32, Hkv=8, d=128,
+                         lens=[1, 300, 4096, 17, 2000, 64, 999, 5], max_blocks=256)
+    t = _args(case)
+    S = len(case.seq_lens)
+    o = torch.empty((S, case.H, case.dv), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((S, case.H), dtype=torch.float32, device="cuda")
+    call = lambda: fb.fa_paged_decode_noalloc(*t[:5], o, lse, S, case.H, case.Hkv, case.d, case.dv,
+                                              case.page_size, case.num_pages, case.max_blocks, 8,
+                                              case.scale)
+    call()
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(5):
+        call()
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, (free0, free1)
+    assert fb.fa_get_device_status() == 0
 
 
 def test_noalloc_rejects_problems_beyond_the_fixed_scratch():

@@ -8,6 +8,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "../../include/fa.h"
 #include "fa_internal.h"
 
@@ -31,21 +33,39 @@ fa_status cuda_fail(cudaError_t e, const char* what) {
 // record timeouts and bad block-table ids there instead of faulting.
 __device__ int g_device_status = 0;
 
-constexpr int kMaxDevices = 64;
-int* g_status_ptr[kMaxDevices] = {nullptr};
+// Its device address belongs to the CUDA context the library's module is
+// loaded in: after cudaDeviceReset, or in a context the caller created
+// itself, the same variable has another address.  Addresses are therefore
+// cached per context id (a few contexts at most), never per device ordinal.
+constexpr int kMaxContexts = 64;
+struct CtxAddr {
+  unsigned long long ctx;
+  int* ptr;
+};
+CtxAddr g_status_cache[kMaxContexts] = {};
+int g_status_next = 0;
+std::mutex g_status_mutex;
 
 fa_status status_ptr(int** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_UNSUPPORTED, "device ordinal %d", dev);
-  if (g_status_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_device_status);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
-    g_status_ptr[dev] = static_cast<int*>(p);
+  std::lock_guard<std::mutex> lock(g_status_mutex);
+  unsigned long long ctx = 0;
+  if (fa::current_context_id(&ctx)) {
+    for (const CtxAddr& c : g_status_cache)
+      if (c.ptr != nullptr && c.ctx == ctx) {
+        *out = c.ptr;
+        return FA_OK;
+      }
   }
-  *out = g_status_ptr[dev];
+  // not seen yet (or no context bound to this thread: the lookup below binds
+  // the runtime's primary context of the current device)
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_device_status);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+  if (fa::current_context_id(&ctx)) {   // else (no context ids) look it up every call
+    g_status_cache[g_status_next] = CtxAddr{ctx, static_cast<int*>(p)};
+    g_status_next = (g_status_next + 1) % kMaxContexts;
+  }
+  *out = static_cast<int*>(p);
   return FA_OK;
 }
 
@@ -164,6 +184,10 @@ fa_status fa_forward_f32(const float* q, const float* k, const float* v, float* 
                          int causal, void* stream) {
   fa_status st = check_dense(q, k, v, o, lse, B, H, Hkv, n, m, d, dv, causal, "fa_forward_f32");
   if (st != FA_OK) return st;
+  // the fp32 kernel takes the row max of the unscaled scores: a non-positive
+  // scale would turn it into a minimum
+  if (!(scale > 0.f) || scale == INFINITY)
+    return fail(FA_ERR_INVALID_ARG, "fa_forward_f32: scale must be positive and finite");
   if (!((d == 64 || d == 128) && (dv == 64 || dv == 128)))
     return fail(FA_ERR_UNSUPPORTED, "fa_forward_f32: d=%d dv=%d (supported: 64, 128)", d, dv);
   // one CTA row block per (query block, head, batch): grid y and z hold H and B
@@ -271,6 +295,8 @@ fa_status fa_paged_decode(const void* q, const void* k_cache, const void* v_cach
     return fail(FA_ERR_INVALID_ARG, "%s: H=%d Hkv=%d (need H %% Hkv == 0)", fn, H, Hkv);
   if (num_splits < 1 || num_splits > 64)
     return fail(FA_ERR_INVALID_ARG, "%s: num_splits=%d outside [1, 64]", fn, num_splits);
+  if (!(scale > 0.f) || scale == INFINITY)
+    return fail(FA_ERR_INVALID_ARG, "%s: scale must be positive and finite", fn);
   if (d != 128 || dv != 128)
     return fail(FA_ERR_UNSUPPORTED, "%s: d=%d dv=%d (supported: 128)", fn, d, dv);
   if (page_size != 16) return fail(FA_ERR_UNSUPPORTED, "%s: page_size=%d (supported: 16)", fn, page_size);

@@ -12,15 +12,23 @@
 // The array is a file-scope __device__ variable, so every GPU that loads the
 // library holds it (kNoAllocScratchBytes) until the process exits.  Host code
 // cannot pass the variable's name to a kernel (on the host it only stands in
-// for the symbol); the device address is looked up once per device, with that
-// device current, by cudaGetSymbolAddress on the first call made on it.
+// for the symbol); its device address is looked up by cudaGetSymbolAddress,
+// with the device current, on the first call made on that device, and kept.
+// The address belongs to the CUDA context the module is loaded in, so it is
+// kept per context id: after a cudaDeviceReset (a new context, where the array
+// has a new address) the next call looks it up again instead of handing the
+// kernels a stale pointer.
 //
-// All calls share the array and it keeps the previous call's contents.  The
-// partials kernel overwrites every (m, l, o) triple the merge reads, so
-// nothing has to be cleared first.  Two calls whose work overlaps on the GPU
-// (other streams, other host threads) race on the array and corrupt each
-// other's results: serialise them.
+// All calls share the array and it keeps the previous call's contents.  When
+// a call completes with the device status clear, the partials kernel has
+// overwritten every (m, l, o) triple the merge reads, so nothing has to be
+// cleared first.  After FA_ERR_TIMEOUT some warps returned without writing
+// their triples and the merge read the previous call's: O and LSE of that
+// call are undefined.  Two calls whose work overlaps on the GPU (other
+// streams, other host threads) race on the array and corrupt each other's
+// results: serialise them.
 #include <cuda_runtime.h>
+#include <math.h>
 #include <mutex>
 #include <stdint.h>
 #include <stdio.h>
@@ -39,30 +47,40 @@ constexpr size_t kNoAllocScratchBytes = FA_NOALLOC_SCRATCH_BYTES;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {nullptr};
+constexpr int kMaxContexts = 64;
+struct ScratchAddr {
+  unsigned long long ctx;
+  void* ptr;
+};
+ScratchAddr g_scratch_addr[kMaxContexts] = {};
+int g_scratch_next = 0;
 std::mutex g_scratch_mutex;
 
-// Device address of the scratch array on the current device (looked up once).
+// Device address of the scratch array in the context current on this thread
+// (the current device's primary context unless the caller bound another).
 fa_status scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return fa::api_fail(FA_ERR_CUDA, "fa_paged_decode_noalloc: cudaGetDevice failed");
-  if (dev < 0 || dev >= kMaxDevices)
-    return fa::api_fail(FA_ERR_UNSUPPORTED, "fa_paged_decode_noalloc: device ordinal out of range");
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || p == nullptr) {
-      char msg[256];
-      snprintf(msg, sizeof(msg), "fa_paged_decode_noalloc: cudaGetSymbolAddress(scratch): %s",
-               cudaGetErrorString(e));
-      return fa::api_fail(FA_ERR_CUDA, msg);
-    }
-    g_scratch_addr[dev] = p;
+  unsigned long long ctx = 0;
+  if (fa::current_context_id(&ctx)) {
+    for (const ScratchAddr& a : g_scratch_addr)
+      if (a.ptr != nullptr && a.ctx == ctx) {
+        *out = a.ptr;
+        return FA_OK;
+      }
   }
-  *out = g_scratch_addr[dev];
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess || p == nullptr) {
+    char msg[256];
+    snprintf(msg, sizeof(msg), "fa_paged_decode_noalloc: cudaGetSymbolAddress(scratch): %s",
+             cudaGetErrorString(e));
+    return fa::api_fail(FA_ERR_CUDA, msg);
+  }
+  if (fa::current_context_id(&ctx)) {   // else (no context ids) look it up every call
+    g_scratch_addr[g_scratch_next] = ScratchAddr{ctx, p};
+    g_scratch_next = (g_scratch_next + 1) % kMaxContexts;
+  }
+  *out = p;
   return FA_OK;
 }
 
@@ -83,6 +101,8 @@ extern "C" fa_status fa_paged_decode_noalloc(const void* q, const void* k_cache,
     return fa::api_fail(FA_ERR_INVALID_ARG, "fa_paged_decode_noalloc: need H > 0, Hkv > 0, H % Hkv == 0");
   if (num_splits < 1 || num_splits > 64)
     return fa::api_fail(FA_ERR_INVALID_ARG, "fa_paged_decode_noalloc: num_splits outside [1, 64]");
+  if (!(scale > 0.f) || scale == INFINITY)
+    return fa::api_fail(FA_ERR_INVALID_ARG, "fa_paged_decode_noalloc: scale must be positive and finite");
   if (d != 128 || dv != 128 || page_size != 16 || H / Hkv > 16)
     return fa::api_fail(FA_ERR_UNSUPPORTED,
                         "fa_paged_decode_noalloc: supported d == dv == 128, page_size 16, H/Hkv <= 16");
@@ -100,6 +120,10 @@ extern "C" fa_status fa_paged_decode_noalloc(const void* q, const void* k_cache,
     return fa::api_fail(FA_ERR_INVALID_ARG, "fa_paged_decode_noalloc: null pointer");
   if (num_pages == 0 || max_blocks_per_seq == 0)
     return fa::api_fail(FA_ERR_INVALID_ARG, "fa_paged_decode_noalloc: empty page pool or block table");
+  // page rows (page * Hkv + head) * 16 are 32-bit in the kernels (the units,
+  // sequences x heads x splits, are bounded by the scratch size above)
+  if ((long long)num_pages * Hkv * 16 > 0x7fffffffLL)
+    return fa::api_fail(FA_ERR_UNSUPPORTED, "fa_paged_decode_noalloc: page pool too large");
   const uintptr_t mis = (reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
                          reinterpret_cast<uintptr_t>(v_cache) | reinterpret_cast<uintptr_t>(o)) & 15u;
   if (mis || (reinterpret_cast<uintptr_t>(lse) & 3u) ||

@@ -2,11 +2,45 @@
 // translation units.  Host-side only; not part of the public ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
 
 namespace fa {
+
+// Id of the CUDA context current on the calling thread (the runtime's primary
+// context of the current device, unless the caller made another current).
+// Device addresses of the library's __device__ variables belong to one
+// context: cudaDeviceReset or another context gives the same variable another
+// address, so a cached address is keyed by this id.  False when no live
+// context is current.  The driver calls are fetched through the runtime, so
+// the library does not link libcuda directly.
+inline bool current_context_id(unsigned long long* id) {
+  typedef CUresult (*GetCurrentFn)(CUcontext*);
+  typedef CUresult (*GetIdFn)(CUcontext, unsigned long long*);
+  struct Fns {
+    GetCurrentFn get_current = nullptr;
+    GetIdFn get_id = nullptr;
+  };
+  static const Fns fns = [] {   // looked up once, thread-safely
+    Fns f;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      f.get_current = reinterpret_cast<GetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      f.get_id = reinterpret_cast<GetIdFn>(p);
+    return f;
+  }();
+  if (fns.get_current == nullptr || fns.get_id == nullptr) return false;
+  CUcontext ctx = nullptr;
+  if (fns.get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  return fns.get_id(ctx, id) == CUDA_SUCCESS;
+}
 
 // Device status codes written by kernels (same values as fa_status).
 enum : int {
