@@ -26,9 +26,12 @@
 // (s * scale * log2 e).  The reference ref is the running max, raised only
 // when a tile's max exceeds it by more than 8 (a factor 256): then acc (O in
 // tensor memory) and l are multiplied by alpha = 2^(m_old - m_new) before the
-// next P V.  Between raises p can reach 256, which bf16 and fp32 hold exactly
-// enough; the final O = acc / l and LSE = (ref + log2 l) ln 2 are exact in
-// any case.  The row max itself is taken only when needed: p is first formed
+// next P V.  Between raises p can reach 256, inside bf16's and fp32's range.
+// Two row sums are kept: l of the exact p, for LSE = (ref + log2 l) ln 2, and
+// l_p of the bf16-rounded p the P V MMA multiplies, for O = acc / l_p, so that
+// O is a weighted mean of V rows whose weights sum to one whatever the
+// rounding (a row one key dominates gets that key's V row back).  The row max
+// itself is taken only when needed: p is first formed
 // against the current ref, and a tile row sum of at most 256 proves no raise
 // is due (see the softmax loop).  While a row has seen only
 // masked keys its reference is 0, so exp(-inf - -inf) never occurs ("S12
@@ -68,9 +71,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 // The reference is raised only when a tile's max passes it by more than the
 // threshold (log2 units), so p stays at most 2^8: e4m3 P saturates at 448.
-// For bf16 a wider threshold (32 was measured) raises less often but leaves
-// the row's largest p off 1.0 more often, and its bf16 rounding then shows in
-// O undivided: the hot ragged workload failed its 2e-2 bound at 2.2e-2.
+// For bf16, O is divided by the sum of the same rounded p, so its accuracy
+// does not depend on the threshold; 12, 16 and 24 measured the same speed.
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kRaiseSum = 256.0f;   // 2^kRescaleThreshold
 
@@ -185,6 +187,54 @@ __device__ __forceinline__ float exp_pass(const uint32_t (&sr)[4][32], uint32_t 
   return ls0 + ls1;
 }
 
+// bf16 form of the pass above: p = 2^(s * scale_log2 - ref) for the 128 keys
+// of sr, packed to bf16 pairs in pp (pp[w] holds keys 2w, 2w+1, key 2w in the
+// low half: the row's 64 P columns in tensor-memory order).  With STORE each
+// chunk of 32 keys goes to tensor memory as soon as it is packed; otherwise the
+// caller stores pp (or discards it).  Returns the row sum of the unrounded p.
+template <bool STORE>
+__device__ __forceinline__ float exp_pack_bf16(const uint32_t (&sr)[4][32], uint32_t s_col,
+                                               uint64_t sc2, uint64_t nref2, uint32_t (&pp)[64]) {
+  uint64_t lsum2[4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) lsum2[a] = ptx::f2_bits(0.f, 0.f);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      const uint64_t x = ptx::ffma2(
+          ptx::f2_bits(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])), sc2, nref2);
+      float x0, x1;
+      ptx::f2_split(x, x0, x1);
+      const float p0 = ptx::ex2(x0);
+      const float p1 = ptx::ex2(x1);
+      lsum2[(e / 2) & 3] = ptx::fadd2(lsum2[(e / 2) & 3], ptx::f2_bits(p0, p1));
+      pp[c * 16 + e / 2] = ptx::pack_bf16x2(p0, p1);
+    }
+    if constexpr (STORE) {
+      uint32_t chunk[16];
+#pragma unroll
+      for (int w = 0; w < 16; ++w) chunk[w] = pp[c * 16 + w];
+      ptx::tmem_st16(s_col + c * 16, chunk);
+    }
+  }
+  float ls0, ls1;
+  ptx::f2_split(ptx::fadd2(ptx::fadd2(lsum2[0], lsum2[1]), ptx::fadd2(lsum2[2], lsum2[3])), ls0, ls1);
+  return ls0 + ls1;
+}
+
+// Row sum of the bf16 P the P V MMA multiplies, in fp32: each bf16 value is
+// added to an fp32 accumulator by one mixed-precision add (exact widening,
+// one rounding), eight independent chains.
+__device__ __forceinline__ float sum_packed_bf16(const uint32_t (&pp)[64]) {
+  float acc[8];
+#pragma unroll
+  for (int a = 0; a < 8; ++a) acc[a] = 0.f;
+#pragma unroll
+  for (int w = 0; w < 64; ++w) ptx::add_bf16x2_to_f32(acc[2 * (w & 3)], acc[2 * (w & 3) + 1], pp[w]);
+  return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+}
+
 // The unit of query pair t (rows 256t .. 256t+255) of sequence b, head h.
 __device__ __forceinline__ Unit make_unit(int b, int h, int t, int H, int Hkv, int n, int m,
                                           int causal, const int* cu_q, const int* cu_k,
@@ -205,7 +255,7 @@ __device__ __forceinline__ Unit make_unit(int b, int h, int t, int H, int Hkv, i
     U.k_row0 = 0;
     U.kv_len = __ldg(seq_lens + U.b);
     U.bad = U.q_row0 < 0 || U.q_len < 0 || U.q_row0 + U.q_len > total_q || U.kv_len < 0 ||
-            U.kv_len > max_blocks * 16;
+            (long long)U.kv_len > (long long)max_blocks * 16;   // wide: max_blocks may pass 2^27
   } else if (cu_q != nullptr) {
     U.q_row0 = __ldg(cu_q + U.b);
     U.q_len = __ldg(cu_q + U.b + 1) - U.q_row0;
@@ -396,12 +446,21 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             uint8_t* tile = sKV + slot * C::kTileBytes;
             const uint32_t dst = ptx::smem_u32(tile);
             const CUtensorMap* map = which == 0 ? &tmK : &tmV;
+            const int rows_valid = min(kBlockN, U.kv_len - j * kBlockN);
+            // A V tile whose rows past the sequence's end hold something else
+            // (a cache page may hold anything; in a packed batch they are the
+            // next sequence's rows) lands on the fix barrier first: those
+            // keys' weights are exactly 0, but 0 * inf and 0 * NaN are NaN,
+            // so the rows are zeroed before the MMA may read the tile.  Dense
+            // tiles need no fix: their 4-D view reads zeros past a batch
+            // element's last row, as the packed view does past the buffer.
+            bool fix = false;
+            if constexpr (PAGED) fix = which == 1 && rows_valid < kBlockN;
+            else if constexpr (VAR)
+              fix = which == 1 && rows_valid < kBlockN && U.k_row0 + U.kv_len < total_k;
+            const uint32_t bar = fix ? bar_fix : bar_kvf + 8 * slot;
             if constexpr (PAGED) {
-              const int rows_valid = min(kBlockN, U.kv_len - j * kBlockN);
               const int npages = (rows_valid + 15) / 16;
-              // a V tile reaching past the end lands on the fix barrier first
-              const bool fix = which == 1 && rows_valid < kBlockN;
-              const uint32_t bar = fix ? bar_fix : bar_kvf + 8 * slot;
               // lane 0 posts the byte count (the barrier's one arrival, so the
               // phase cannot complete before it), then lane pg looks up page
               // pg and issues its boxes: the page copies go out in parallel
@@ -419,33 +478,36 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 for (int c = 0; c < C::kChunks; ++c)
                   ptx::tma_load_2d(dst + c * 16384 + pg * 2048, map, C::kChunkElems * c, row, bar);
               }
-              if (fix) {
-                fix_pending = true;
-                if (!(ok = ptx::mbar_wait(bar_fix, nfix & 1, status, abort_flag))) break;
-                fix_pending = false;
-                ++nfix;
-                // rows past the end: whatever the cache holds there (NaN
-                // included) must not reach P V, where 0 * NaN = NaN
-                const int zero_rows = kBlockN - rows_valid;
-                for (int idx = lane; idx < zero_rows * 8 * C::kChunks; idx += 32) {
-                  const int c = idx / (zero_rows * 8);
-                  const int rem = idx % (zero_rows * 8);
-                  const int row = rows_valid + rem / 8;
-                  *reinterpret_cast<uint4*>(tile + c * 16384 + row * 128 + (rem % 8) * 16) =
-                      make_uint4(0u, 0u, 0u, 0u);
-                }
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar_kvf + 8 * slot);
-              }
             } else {
               if (lane == 0) {
-                ptx::mbar_arrive_expect_tx(bar_kvf + 8 * slot, C::kTileBytes);
+                ptx::mbar_arrive_expect_tx(bar, C::kTileBytes);
 #pragma unroll
-                for (int c = 0; c < C::kChunks; ++c)
-                  ptx::tma_load_3d_hint(dst + c * 16384, map, C::kChunkElems * c, U.hk,
-                                        U.k_row0 + j * kBlockN, bar_kvf + 8 * slot, pol_kv);
+                for (int c = 0; c < C::kChunks; ++c) {
+                  if constexpr (VAR)
+                    ptx::tma_load_3d_hint(dst + c * 16384, map, C::kChunkElems * c, U.hk,
+                                          U.k_row0 + j * kBlockN, bar, pol_kv);
+                  else
+                    ptx::tma_load_4d_hint(dst + c * 16384, map, C::kChunkElems * c, U.hk,
+                                          j * kBlockN, U.b, bar, pol_kv);
+                }
               }
+            }
+            if (fix) {
+              fix_pending = true;
+              if (!(ok = ptx::mbar_wait(bar_fix, nfix & 1, status, abort_flag))) break;
+              fix_pending = false;
+              ++nfix;
+              const int zero_rows = kBlockN - rows_valid;
+              for (int idx = lane; idx < zero_rows * 8 * C::kChunks; idx += 32) {
+                const int c = idx / (zero_rows * 8);
+                const int rem = idx % (zero_rows * 8);
+                const int row = rows_valid + rem / 8;
+                *reinterpret_cast<uint4*>(tile + c * 16384 + row * 128 + (rem % 8) * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+              }
+              ptx::fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) ptx::mbar_arrive(bar_kvf + 8 * slot);
             }
             ++li;
           }
@@ -600,30 +662,35 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       const int nkv = U.n_kv[i];
       float m_ref = -INFINITY;   // running reference (log2 units)
       bool max_first = false;    // this warp forms P max-first for the rest of the unit
-      float l_run = 0.f;
+      float l_run = 0.f;         // sum of the unrounded p: the LSE's l
+      float l_p = 0.f;           // bf16: sum of the rounded p the P V MMA used (O's divisor)
       for (int j = 0; j < nkv; ++j) {
         // warp-uniform outcome: the tcgen05.ld/st below are warp-collective
         ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar_s + 8 * i, ns & 1, status, abort_flag));
         if (!ok) break;
         ++ns;
         ptx::tc_fence_after();
-        uint32_t sr[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) ptx::tmem_ld32(s_col + c * 32, sr[c]);
-        ptx::tmem_wait_ld();
         // mask keys past the end and, causal, keys j > qi + (m - n): only tiles
         // that reach past the end or past the tile's first row's diagonal
         const int k0 = j * kBlockN;
         const int diag = q_start + (U.kv_len - U.q_len);   // last key row q_start sees
-        if (k0 + kBlockN > U.kv_len || (causal && k0 + kBlockN - 1 > diag)) {
-          int vis = U.kv_len - k0;
-          if (causal) vis = min(vis, qi + (U.kv_len - U.q_len) - k0 + 1);
+        const bool masked = k0 + kBlockN > U.kv_len || (causal && k0 + kBlockN - 1 > diag);
+        int vis = U.kv_len - k0;
+        if (causal) vis = min(vis, qi + (U.kv_len - U.q_len) - k0 + 1);
+        uint32_t sr[4][32];
+        auto load_s = [&]() {
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 4; ++c) ptx::tmem_ld32(s_col + c * 32, sr[c]);
+          ptx::tmem_wait_ld();
+          if (masked) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (c * 32 + e >= vis) sr[c][e] = __float_as_uint(-INFINITY);
-        }
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if (c * 32 + e >= vis) sr[c][e] = __float_as_uint(-INFINITY);
+          }
+        };
+        load_s();
         // From the second tile on, P is first formed against the current
         // reference without the row max.  Every p is at most the tile's row
         // sum, so a sum of at most 2^threshold shows that no score passed the
@@ -635,14 +702,23 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // with a few dominant keys), and each costs a second pass.  Measured
         // on the hot ragged workload (d=128): 715 TFLOP/s retrying every tile,
         // 786 going max-first for 4 tiles, 821 for the rest of the unit.
+        // (bf16: the first attempt stores nothing, so on a miss S is still
+        // whole in tensor memory and is loaded again instead of being kept in
+        // registers beside the packed P.)
         const uint64_t sc2 = ptx::f2_bits(scale_log2, scale_log2);
         float lsum = 0.f;
         bool full = true;
+        uint32_t pp[64];   // bf16: this tile's packed P
         if (j > 0 && !max_first) {
           const float ref = m_ref == -INFINITY ? 0.f : m_ref;
-          lsum = exp_pass<FP8>(sr, s_col, sc2, ptx::f2_bits(-ref, -ref));
+          if constexpr (FP8) lsum = exp_pass<true>(sr, s_col, sc2, ptx::f2_bits(-ref, -ref));
+          else lsum = exp_pack_bf16<false>(sr, s_col, sc2, ptx::f2_bits(-ref, -ref), pp);
           full = __any_sync(0xffffffffu, !(lsum <= kRaiseSum) || m_ref == -INFINITY);
           max_first = full;
+          if constexpr (!FP8) {
+            if (full) load_s();
+            else ptx::tmem_st64(s_col, pp);
+          }
         }
         if (full) {
           const float m_tile = row_max(sr) * scale_log2;   // scale > 0: max commutes with it
@@ -653,6 +729,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             alpha = m_ref == -INFINITY ? 1.f : ptx::ex2(m_ref - m_tile);
             m_ref = m_tile;
             l_run *= alpha;
+            l_p *= alpha;
           }
           const float ref = m_ref == -INFINITY ? 0.f : m_ref;
           // rescale acc when this warp raised a reference after the first
@@ -668,13 +745,20 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
               ptx::tmem_st32(o_col + c * 32, ov);
             }
           }
-          lsum = exp_pass<FP8>(sr, s_col, sc2, ptx::f2_bits(-ref, -ref));
+          if constexpr (FP8) lsum = exp_pass<true>(sr, s_col, sc2, ptx::f2_bits(-ref, -ref));
+          else lsum = exp_pack_bf16<true>(sr, s_col, sc2, ptx::f2_bits(-ref, -ref), pp);
         }
         // all of P_i sits in tensor memory: hand it to the MMA warp
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar_p + 8 * i);
         l_run += lsum;
+        // O is divided by the sum of the p the MMA multiplied (rounded to
+        // bf16), not by the exact sum: then a row that one key dominates gets
+        // that key's V row back to within fp32 rounding, where the exact sum
+        // would leave the rounding of that key's p (up to 2^-8 relative) in O.
+        // Done after the hand-off, while the MMAs run.
+        if constexpr (!FP8) l_p += sum_packed_bf16(pp);
       }
       if (!ok) break;
 
@@ -701,7 +785,10 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       }
       // O has total_q * H rows of D (dense: total_q = B * n); LSE as many entries
       if (row_valid && FA_IN_BOUNDS(orow, (size_t)total_q * H, status)) {
-        const float inv = l_run > 0.f ? out_scale / l_run : 0.f;
+        // O's divisor (bf16: the rounded sum, positive exactly when l_run is:
+        // a normal fp32 p rounds to a normal bf16) and the LSE's l
+        const float l_o = FP8 ? l_run : l_p;
+        const float inv = l_o > 0.f ? out_scale / l_o : 0.f;
         uint4* dst = reinterpret_cast<uint4*>(o + orow * D);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c)
@@ -759,11 +846,24 @@ cudaError_t launch(const FwdParams& p, cudaStream_t stream, const char** why) {
       *why = "tensor map for the k/v caches";
       return cudaErrorInvalidValue;
     }
-  } else {
+  } else if (varlen) {
     const uint64_t dims[3] = {(uint64_t)D, (uint64_t)p.Hkv, k_rows > 0 ? k_rows : 1};
     const uint64_t strides[2] = {(uint64_t)C::kRowBytes, (uint64_t)p.Hkv * C::kRowBytes};
     if (!make_tmap_bf16(&tk, p.m > 0 ? p.k : p.q, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, dt) ||
         !make_tmap_bf16(&tv, p.m > 0 ? p.v : p.q, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, dt)) {
+      *why = "tensor map for k/v";
+      return cudaErrorInvalidValue;
+    }
+  } else {
+    // 4-D views (dim, head, token row, batch element) of dense K and V: a
+    // tile past an element's last row reads zeros, never the next element
+    const uint64_t m_rows = p.m > 0 ? (uint64_t)p.m : 1;
+    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)p.Hkv, m_rows, (uint64_t)p.B};
+    const uint64_t strides[3] = {(uint64_t)C::kRowBytes, (uint64_t)p.Hkv * C::kRowBytes,
+                                 m_rows * p.Hkv * C::kRowBytes};
+    const uint32_t box4[4] = {(uint32_t)C::kChunkElems, 1, 128, 1};
+    if (!make_tmap_bf16(&tk, p.m > 0 ? p.k : p.q, 4, dims, strides, box4, CU_TENSOR_MAP_SWIZZLE_128B, dt) ||
+        !make_tmap_bf16(&tv, p.m > 0 ? p.v : p.q, 4, dims, strides, box4, CU_TENSOR_MAP_SWIZZLE_128B, dt)) {
       *why = "tensor map for k/v";
       return cudaErrorInvalidValue;
     }
