@@ -72,10 +72,10 @@ typedef enum {
  *   scale  multiplies Q K^T; must be positive and finite (pass 1/sqrt(d)
  *          for the usual attention)
  *   causal 0 or 1
- * Non-finite inputs: the last K/V tile of a batch element may reach into the
- * next element's rows.  Those keys are masked (their weights are exactly 0),
- * but 0 * inf is NaN, so an inf or NaN in the next element's V reaches this
- * element's output too (it already makes that element's own output NaN).
+ * Non-finite inputs stay in their own batch element: the last K/V tile of an
+ * element whose m is not a multiple of the tile reads zeros past its last row
+ * (never the next element's rows, whose inf or NaN would otherwise turn the
+ * masked keys' zero weights into NaN: 0 * inf = NaN).
  * Supported: d == dv, d in {64, 128}; pointers 16-byte aligned; n, m >= 0;
  * B*n, B*m and H*n below 2^31 (token rows and the LSE stride are 32-bit).
  * Computes S = Q K^T and P V on the tcgen05 tensor cores (bf16 operands,
@@ -105,10 +105,16 @@ fa_status fa_forward_fp8(const void* q, const void* k, const void* v, void* o, f
 
 /*
  * fa_forward_f32 — fp32 attention forward, dense batch; same shapes, layouts
- * and semantics as fa_forward with every tensor in float32.  Arithmetic is
- * IEEE fp32 on the CUDA cores (no TF32); each score is carried as a
- * compensated (hi, lo) pair so that exp(s - m) keeps fp32 relative accuracy
- * when the scores are in the hundreds.
+ * and semantics as fa_forward with every tensor in float32.
+ * Passage: "手搓 Attention" §1 (shapes and scale), §4 version 2 (subtract the
+ * row maximum before exp; in fp32 that keeps hot scores of several hundred
+ * finite and within a few 1e-6 of float64) and §7 version 4 (the recurrence).
+ * Arithmetic is IEEE fp32 on the CUDA cores (no TF32); each score is carried
+ * as a compensated (hi, lo) pair so that exp(s - m) keeps fp32 relative
+ * accuracy when the scores are in the hundreds.
+ *   scale  must be positive and finite, as for fa_forward (the row maximum is
+ *          taken on the unscaled scores, which is the scaled maximum only for
+ *          a positive scale); anything else returns FA_ERR_INVALID_ARG
  * Supported: d, dv in {64, 128}; pointers 16-byte aligned; H, B <= 65535.
  */
 fa_status fa_forward_f32(const float* q, const float* k, const float* v, float* o, float* lse,
@@ -119,6 +125,11 @@ fa_status fa_forward_f32(const float* q, const float* k, const float* v, float* 
  * fa_forward_varlen — bf16 attention forward over packed sequences of
  * different lengths.  Sequence s owns query tokens [cu_seqlens_q[s],
  * cu_seqlens_q[s+1]) and key tokens [cu_seqlens_k[s], cu_seqlens_k[s+1]).
+ * Passage: each sequence is its own attention problem ("手搓 Attention" §1),
+ * computed by the same recurrence (§7 version 4; "S12 FlashAttention", 解法)
+ * over that sequence's K/V tiles only; a sequence whose length is not a
+ * multiple of the tile ends on a partly masked tile, and rows whose first
+ * tiles are fully masked take the guard of "S12 FlashAttention", 实现.
  *
  *   q    bf16 [total_q][H][d],  k bf16 [total_k][Hkv][d],  v bf16 [total_k][Hkv][dv]
  *   o    bf16 [total_q][H][dv]  written
@@ -132,9 +143,10 @@ fa_status fa_forward_f32(const float* q, const float* k, const float* v, float* 
  *   max_seqlen_q, max_seqlen_k  upper bounds of the per-sequence lengths
  *        (sizes the launch grid; a larger value only launches idle blocks)
  * Supported as fa_forward; causal uses each sequence's own q and k lengths.
- * Non-finite V rows of one sequence can reach the previous sequence's output
- * as in fa_forward.  (The paged paths zero the V rows past a sequence's end,
- * since a cache page may hold anything there.)
+ * Non-finite values stay in their own sequence: the V rows past a sequence's
+ * end in its last K/V tile (the next sequence's rows) are zeroed in shared
+ * memory before P V, as the paged paths do with the rows past a sequence's
+ * end in its last page.
  */
 fa_status fa_forward_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
                             const int* cu_seqlens_q, const int* cu_seqlens_k, int num_seqs,
@@ -178,9 +190,14 @@ fa_status fa_paged_prefill(const void* q, const void* k_cache, const void* v_cac
                            int max_blocks_per_seq, float scale, int causal, void* stream);
 
 /*
- * fa_paged_decode_workspace_size — bytes of workspace fa_paged_decode needs:
- * the per-split partial triples (m, l: fp32 [num_seqs][H][num_splits] each;
- * o: fp32 [num_seqs][H][num_splits][dv]), each array 256-byte aligned.
+ * fa_paged_decode_workspace_size — bytes of workspace fa_paged_decode and
+ * fa_paged_decode_fused need: the fused form's ticket words first (int32
+ * [num_seqs][H], at the same offset for every split count), then the
+ * per-split partial triples (m, l: fp32 [num_seqs][H][num_splits] each; o:
+ * fp32 [num_seqs][H][num_splits][dv]), each array 256-byte aligned.
+ * Passage: "S12 FlashAttention", 它还解锁了什么 and 练习 1 (flash-decoding:
+ * each split of the keys leaves one (m, l, o) triple per query head, and the
+ * merge reads them all).
  * Returns 0 on invalid sizes.
  */
 size_t fa_paged_decode_workspace_size(int num_seqs, int H, int dv, int num_splits);
@@ -202,6 +219,7 @@ size_t fa_paged_decode_workspace_size(int num_seqs, int H, int dv, int num_split
  *   lse          fp32 [num_seqs][H]      written (may be NULL)
  *   num_splits   1..64: split x of a sequence with P pages covers logical
  *                pages [ceil(x*P/X), ceil((x+1)*P/X)); empty splits are allowed
+ *   scale        positive and finite (else FA_ERR_INVALID_ARG)
  *   workspace    device scratch of at least fa_paged_decode_workspace_size()
  *                bytes, 256-byte aligned; the call writes the partials there
  *                and then merges them (fa_split_combine) on the same stream.
@@ -220,6 +238,32 @@ fa_status fa_paged_decode(const void* q, const void* k_cache, const void* v_cach
                           void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * fa_paged_decode_fused — fa_paged_decode in one launch.
+ * Passage: "S12 FlashAttention", 接下来 (fuse the small-batch decode) and
+ * 练习 1 (the split triples merge with the recurrence's rescale).
+ *
+ * Same arguments, layouts, supported sizes and device status as
+ * fa_paged_decode, and the same O and LSE bits.  The merge runs inside the
+ * decode launch: each (sequence, kv head, split) unit writes its triple,
+ * then takes an atomic ticket of its (sequence, kv head); the unit that takes
+ * the last ticket merges the triples of the group's query heads.  No unit
+ * waits for another.
+ *   workspace  as fa_paged_decode (the same size query).  Its ticket words
+ *              must be zero before the first call that uses this workspace
+ *              (cudaMemset the whole workspace to 0 once after allocating
+ *              it); every call, also one that ends with FA_ERR_TIMEOUT,
+ *              leaves them zero again.  Calls on one workspace must not
+ *              overlap on the GPU.  (fa_paged_decode ignores the ticket
+ *              words, so one workspace may serve both entries.)
+ * After FA_ERR_TIMEOUT, O and LSE are undefined, as for fa_paged_decode.
+ */
+fa_status fa_paged_decode_fused(const void* q, const void* k_cache, const void* v_cache,
+                                const int* block_table, const int* seq_lens, void* o, float* lse,
+                                int num_seqs, int H, int Hkv, int d, int dv, int page_size,
+                                int num_pages, int max_blocks_per_seq, int num_splits, float scale,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * fa_paged_decode_noalloc — fa_paged_decode for callers that cannot allocate.
  * The pages have no counterpart for this call: it exists for library users.
  *
@@ -233,14 +277,19 @@ fa_status fa_paged_decode(const void* q, const void* k_cache, const void* v_cach
  * nothing; the caller still owns and passes every input and output.
  *   - Every GPU that loads the library holds that array until the process ends.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current) and keeps it; make
+ *     that first call before any stream capture.  The address is kept per
+ *     CUDA context: after cudaDeviceReset the next call is again a first
+ *     call (it looks the new address up), so make it outside a capture too.
  *   - A problem whose partials (fa_paged_decode_workspace_size) exceed the
  *     array is rejected with FA_ERR_WORKSPACE before anything is launched.
- *   - All calls share the array, which keeps the last call's contents (every
- *     partial the merge reads is rewritten, so nothing needs clearing).  Calls
- *     that overlap on the GPU (other streams, other threads) race on it and
- *     corrupt each other: serialise them.
+ *   - All calls share the array, which keeps the last call's contents.  A
+ *     call that ends with the device status clear has rewritten every partial
+ *     its merge read, so nothing needs clearing.  After FA_ERR_TIMEOUT some
+ *     partials were not rewritten and the merge read the previous call's:
+ *     that call's O and LSE are undefined.  Calls that overlap on the GPU
+ *     (other streams, other threads) race on the array and corrupt each
+ *     other: serialise them.
  * Arguments, layouts, supported sizes and device status as fa_paged_decode.
  */
 #define FA_NOALLOC_SCRATCH_BYTES (16u << 20)

@@ -294,3 +294,83 @@ def test_wait_timeout_sets_status_and_context_stays_usable(monkeypatch):
     assert fb.fa_get_device_status() == 0
     o_ref, lse_ref = _oracle(case)
     assert_close(host(o), o_ref, BF16_MAX_ABS, BF16_MEAN_ABS)
+
+
+# ------------------------------------------------------------ fused form
+def _bits(x):
+    return x.view(torch.int16 if x.dtype == torch.bfloat16 else torch.int32).cpu().numpy()
+
+
+def _fused(case, splits, ws):
+    return fb.paged_decode_fused(dev(case.q), dev(case.k_cache), dev(case.v_cache),
+                                 dev_i32(case.block_table), dev_i32(case.seq_lens), splits,
+                                 case.scale, workspace=ws)
+
+
+def test_fused_decode_gives_the_two_launch_bits_across_calls():
+    """fa_paged_decode_fused ("S12 FlashAttention", 接下来: fuse the
+    small-batch decode) runs the same partials and, in the split that takes
+    the last ticket, the same merge: O and LSE equal fa_paged_decode's bit for
+    bit.  One workspace (zeroed once) serves every call, with the split count
+    changing from call to call, so the ticket words must come back to zero."""
+    lens = [0, 1, 15, 16, 17, 100, 257, 640]
+    case = I.decode_case(5, num_seqs=len(lens), H=32, Hkv=8, d=128, lens=lens, max_blocks=48)
+    need = fb.fa_paged_decode_workspace_size(len(lens), 32, 128, 64)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    o_ref, lse_ref = _oracle(case)
+    for splits in (1, 3, 4, 8, 16, 64, 8, 5):
+        o, lse = _fused(case, splits, ws)
+        o2, lse2 = _gpu_decode(case, splits)
+        torch.cuda.synchronize()
+        assert np.array_equal(_bits(o), _bits(o2)), f"O bits, X={splits}"
+        assert np.array_equal(_bits(lse), _bits(lse2)), f"LSE bits, X={splits}"
+        assert_close(host(o), o_ref, BF16_MAX_ABS, BF16_MEAN_ABS, what=f"fused X={splits}")
+        assert_lse_close(host(lse), lse_ref, what=f"fused lse X={splits}")
+        assert fb.fa_get_device_status() == 0
+
+
+@pytest.mark.parametrize("group", [1, 4, 16])
+def test_fused_decode_group_sizes(group):
+    case = I.decode_case(6, num_seqs=3, H=2 * group, Hkv=2, d=128, lens=[33, 200, 511],
+                         max_blocks=40)
+    ws = torch.zeros(fb.fa_paged_decode_workspace_size(3, 2 * group, 128, 4), dtype=torch.uint8,
+                     device="cuda")
+    o, lse = _fused(case, 4, ws)
+    o_ref, lse_ref = _oracle(case)
+    assert_close(host(o), o_ref, BF16_MAX_ABS, BF16_MEAN_ABS, what=f"fused group {group}")
+    assert_lse_close(host(lse), lse_ref)
+    assert fb.fa_get_device_status() == 0
+
+
+def test_fused_c4_full_size():
+    """The 64-sequence workload at 4, 8 and 16 splits through one workspace:
+    every output against the oracle and bit for bit against the two-launch form."""
+    case = _c4()
+    o_ref, lse_ref = _c4_ref()
+    ws = torch.zeros(fb.fa_paged_decode_workspace_size(64, 32, 128, 16), dtype=torch.uint8,
+                     device="cuda")
+    for splits in (4, 8, 16):
+        o, lse = _fused(case, splits, ws)
+        o2, lse2 = _gpu_decode(case, splits)
+        torch.cuda.synchronize()
+        assert np.array_equal(_bits(o), _bits(o2)) and np.array_equal(_bits(lse), _bits(lse2))
+        assert_close(host(o), o_ref, BF16_MAX_ABS, BF16_MEAN_ABS, what=f"fused c4 X={splits}")
+        assert_lse_close(host(lse), lse_ref)
+    assert fb.fa_get_device_status() == 0
+
+
+def test_fused_timeout_keeps_the_tickets_consistent(monkeypatch):
+    """A fused call whose warps time out (test hook, no fault) still takes
+    every ticket, so the next call on the same workspace merges correctly."""
+    case = I.decode_case(13, num_seqs=2, H=8, Hkv=2, d=128, lens=[100, 300], max_blocks=24)
+    ws = torch.zeros(fb.fa_paged_decode_workspace_size(2, 8, 128, 3), dtype=torch.uint8,
+                     device="cuda")
+    monkeypatch.setenv("FA_TEST_FORCE_WAIT_TIMEOUT", "1")
+    _fused(case, 3, ws)
+    assert fb.fa_get_device_status() == fb.FA_ERR_TIMEOUT
+    monkeypatch.delenv("FA_TEST_FORCE_WAIT_TIMEOUT")
+    o, lse = _fused(case, 3, ws)
+    assert fb.fa_get_device_status() == 0
+    o_ref, lse_ref = _oracle(case)
+    assert_close(host(o), o_ref, BF16_MAX_ABS, BF16_MEAN_ABS)
+    assert_lse_close(host(lse), lse_ref)

@@ -112,8 +112,10 @@ def test_decode_workspace_size(lib):
     S, H, dv, X = 64, 32, 128, 16
     tri = S * H * X
     r = lambda x: (x + 255) // 256 * 256
-    assert fb.fa_paged_decode_workspace_size(S, H, dv, X) == 2 * r(tri * 4) + r(tri * dv * 4)
-    assert fb.fa_paged_decode_workspace_size(0, H, dv, X) == 0 + 0
+    # the fused form's ticket words, then partial m, l, o
+    assert fb.fa_paged_decode_workspace_size(S, H, dv, X) == \
+        r(S * H * 4) + 2 * r(tri * 4) + r(tri * dv * 4)
+    assert fb.fa_paged_decode_workspace_size(0, H, dv, X) == 0
     assert fb.fa_paged_decode_workspace_size(S, 0, dv, X) == 0
 
 
@@ -141,6 +143,24 @@ def test_decode_validation(lib):
     # 32-bit page rows and unit counts
     assert _dec(lib, P=1 << 25) == fb.FA_ERR_UNSUPPORTED
     assert _dec(lib, S=1 << 26, X=64) == fb.FA_ERR_UNSUPPORTED
+
+
+def test_fused_decode_validation(lib):
+    """fa_paged_decode_fused checks its arguments exactly as fa_paged_decode."""
+    def fused(**kw):
+        a = dict(q=16, kc=16, vc=16, bt=16, sl=16, o=16, lse=16, S=4, H=32, Hkv=8, d=128, dv=128,
+                 page=16, P=100, maxb=8, X=4, scale=0.1, ws=256, wsb=1 << 20)
+        a.update(kw)
+        return lib.fa_paged_decode_fused(a["q"], a["kc"], a["vc"], a["bt"], a["sl"], a["o"],
+                                         a["lse"], a["S"], a["H"], a["Hkv"], a["d"], a["dv"],
+                                         a["page"], a["P"], a["maxb"], a["X"], a["scale"], a["ws"],
+                                         a["wsb"], None)
+    for kw in (dict(X=0), dict(X=65), dict(H=30), dict(page=32), dict(d=64, dv=64),
+               dict(H=64, Hkv=2), dict(ws=None), dict(wsb=100), dict(ws=272), dict(bt=None),
+               dict(P=1 << 25), dict(S=1 << 26, X=64), dict(scale=0.0), dict(scale=float("nan"))):
+        assert fused(**kw) == _dec(lib, **kw), kw
+        assert fused(**kw) != fb.FA_OK, kw
+    assert fused(S=0) == fb.FA_OK
 
 
 def _noalloc(lib, **kw):

@@ -8,8 +8,8 @@ raises FaError with the library's message.  There is no fallback: if the
 library is missing or cannot be loaded, the first call raises.
 
 The helpers at the end (``forward``, ``forward_f32``, ``forward_varlen``,
-``paged_decode``, ``split_combine``) allocate outputs with torch and then call
-the same entry points.
+``paged_decode``, ``paged_decode_fused``, ``split_combine``) allocate outputs
+with torch and then call the same entry points.
 """
 from __future__ import annotations
 
@@ -33,7 +33,7 @@ FA_ERR_DEBUG_CHECK = 7
 
 EXPORTED = ("fa_forward", "fa_forward_fp8", "fa_forward_f32", "fa_forward_varlen", "fa_paged_prefill",
             "fa_paged_decode_workspace_size",
-            "fa_paged_decode", "fa_paged_decode_noalloc", "fa_paged_gather", "fa_split_combine",
+            "fa_paged_decode", "fa_paged_decode_fused", "fa_paged_decode_noalloc", "fa_paged_gather", "fa_split_combine",
             "fa_last_error",
             "fa_get_device_status")
 FA_NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -68,6 +68,7 @@ def load(path: str = LIB_PATH):
         lib.fa_paged_decode_workspace_size.argtypes = [I, I, I, I]
         lib.fa_paged_decode_workspace_size.restype = Z
         lib.fa_paged_decode.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, P, Z, P]
+        lib.fa_paged_decode_fused.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, P, Z, P]
         lib.fa_paged_decode_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, P]
         lib.fa_paged_gather.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, P]
         lib.fa_split_combine.argtypes = [P, P, P, P, P, I, I, I, I, P]
@@ -76,7 +77,7 @@ def load(path: str = LIB_PATH):
         lib.fa_get_device_status.argtypes = [P, ctypes.POINTER(I)]
         for name in ("fa_forward", "fa_forward_fp8", "fa_forward_f32", "fa_forward_varlen",
                      "fa_paged_prefill",
-                     "fa_paged_decode",
+                     "fa_paged_decode", "fa_paged_decode_fused",
                      "fa_paged_decode_noalloc", "fa_paged_gather", "fa_split_combine",
                      "fa_get_device_status"):
             getattr(lib, name).restype = I
@@ -154,6 +155,16 @@ def fa_paged_decode(q, k_cache, v_cache, block_table, seq_lens, o, lse, num_seqs
                                   _p(o), _p(lse), num_seqs, H, Hkv, d, dv, page_size, num_pages,
                                   max_blocks_per_seq, num_splits, float(scale), _p(workspace),
                                   int(workspace_bytes), _stream(stream)))
+
+
+def fa_paged_decode_fused(q, k_cache, v_cache, block_table, seq_lens, o, lse, num_seqs, H, Hkv, d,
+                          dv, page_size, num_pages, max_blocks_per_seq, num_splits, scale,
+                          workspace, workspace_bytes, stream=None):
+    _check(load().fa_paged_decode_fused(_p(q), _p(k_cache), _p(v_cache), _p(block_table),
+                                        _p(seq_lens), _p(o), _p(lse), num_seqs, H, Hkv, d, dv,
+                                        page_size, num_pages, max_blocks_per_seq, num_splits,
+                                        float(scale), _p(workspace), int(workspace_bytes),
+                                        _stream(stream)))
 
 
 def fa_paged_decode_noalloc(q, k_cache, v_cache, block_table, seq_lens, o, lse, num_seqs, H, Hkv,
@@ -271,6 +282,24 @@ def paged_decode(q, k_cache, v_cache, block_table, seq_lens, num_splits, scale, 
     return o, lse
 
 
+def paged_decode_fused(q, k_cache, v_cache, block_table, seq_lens, num_splits, scale,
+                       workspace=None, stream=None):
+    """As paged_decode, in one launch; a workspace passed in must have had its
+    ticket words zeroed once (a new one is zeroed here)."""
+    import torch
+    S, H, d = q.shape
+    P, Hkv, page, dv = v_cache.shape
+    need = fa_paged_decode_workspace_size(S, H, dv, num_splits)
+    if workspace is None:
+        workspace = torch.zeros(max(need, 1), dtype=torch.uint8, device=q.device)
+    o = torch.empty((S, H, dv), dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((S, H), dtype=torch.float32, device=q.device)
+    fa_paged_decode_fused(q, k_cache, v_cache, block_table, seq_lens, o, lse, S, H, Hkv, d, dv,
+                          page, P, block_table.shape[1], num_splits, scale, workspace,
+                          workspace.numel(), stream)
+    return o, lse
+
+
 def split_combine(part_m, part_l, part_o, stream=None):
     import torch
     S, H, X, dv = part_o.shape
@@ -287,7 +316,7 @@ def decode_workspace_views(workspace, num_seqs, H, dv, num_splits):
     def r256(x):
         return (x + 255) // 256 * 256
     tri = num_seqs * H * num_splits
-    ws = workspace.view(torch.uint8)
+    ws = workspace.view(torch.uint8)[r256(num_seqs * H * 4):]   # past the ticket words
     a = r256(tri * 4)
     pm = ws[:tri * 4].view(torch.float32).view(num_seqs, H, num_splits)
     pl = ws[a:a + tri * 4].view(torch.float32).view(num_seqs, H, num_splits)

@@ -280,15 +280,24 @@ static size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 size_t fa_paged_decode_workspace_size(int num_seqs, int H, int dv, int num_splits) {
   if (num_seqs < 0 || H <= 0 || dv <= 0 || num_splits <= 0) return 0;
   const size_t tri = (size_t)num_seqs * H * num_splits;
-  return 2 * round256(tri * sizeof(float)) + round256(tri * dv * sizeof(float));
+  // the fused form's ticket counters first (one per (sequence, head) bounds
+  // the one per (sequence, kv head) it uses; at a fixed offset, so zeroed
+  // once they serve every split count), then partial m, l and o
+  return round256((size_t)num_seqs * H * sizeof(int)) + 2 * round256(tri * sizeof(float)) +
+         round256(tri * dv * sizeof(float));
 }
 
-fa_status fa_paged_decode(const void* q, const void* k_cache, const void* v_cache,
-                          const int* block_table, const int* seq_lens, void* o, float* lse,
-                          int num_seqs, int H, int Hkv, int d, int dv, int page_size,
-                          int num_pages, int max_blocks_per_seq, int num_splits, float scale,
-                          void* workspace, size_t workspace_bytes, void* stream) {
-  const char* fn = "fa_paged_decode";
+}  // extern "C"
+
+namespace {
+
+// Argument checks and workspace carving shared by the two decode entries.
+fa_status decode_setup(const char* fn, const void* q, const void* k_cache, const void* v_cache,
+                       const int* block_table, const int* seq_lens, void* o, float* lse,
+                       int num_seqs, int H, int Hkv, int d, int dv, int page_size, int num_pages,
+                       int max_blocks_per_seq, int num_splits, float scale, void* workspace,
+                       size_t workspace_bytes, fa::DecodeParams* p, bool* nothing) {
+  *nothing = false;
   if (num_seqs < 0 || num_pages < 0 || max_blocks_per_seq < 0)
     return fail(FA_ERR_INVALID_ARG, "%s: negative size", fn);
   if (H <= 0 || Hkv <= 0 || H % Hkv != 0)
@@ -301,7 +310,10 @@ fa_status fa_paged_decode(const void* q, const void* k_cache, const void* v_cach
     return fail(FA_ERR_UNSUPPORTED, "%s: d=%d dv=%d (supported: 128)", fn, d, dv);
   if (page_size != 16) return fail(FA_ERR_UNSUPPORTED, "%s: page_size=%d (supported: 16)", fn, page_size);
   if (H / Hkv > 16) return fail(FA_ERR_UNSUPPORTED, "%s: H/Hkv=%d > 16", fn, H / Hkv);
-  if (num_seqs == 0) return FA_OK;
+  if (num_seqs == 0) {
+    *nothing = true;
+    return FA_OK;
+  }
   if (q == nullptr || o == nullptr || block_table == nullptr || seq_lens == nullptr ||
       k_cache == nullptr || v_cache == nullptr)
     return fail(FA_ERR_INVALID_ARG, "%s: null pointer", fn);
@@ -325,18 +337,59 @@ fa_status fa_paged_decode(const void* q, const void* k_cache, const void* v_cach
   if (st != FA_OK) return st;
   const size_t tri = (size_t)num_seqs * H * num_splits;
   char* ws = static_cast<char*>(workspace);
+  int* tickets = reinterpret_cast<int*>(ws);
+  ws += round256((size_t)num_seqs * H * sizeof(int));
   float* part_m = reinterpret_cast<float*>(ws);
   float* part_l = reinterpret_cast<float*>(ws + round256(tri * sizeof(float)));
   float* part_o = reinterpret_cast<float*>(ws + 2 * round256(tri * sizeof(float)));
-  fa::DecodeParams p{q, k_cache, v_cache, block_table, seq_lens, num_seqs, H, Hkv, d, dv,
-                     page_size, num_pages, max_blocks_per_seq, num_splits, scale,
-                     part_m, part_l, part_o, sp};
+  *p = fa::DecodeParams{q, k_cache, v_cache, block_table, seq_lens, num_seqs, H, Hkv, d, dv,
+                        page_size, num_pages, max_blocks_per_seq, num_splits, scale,
+                        part_m, part_l, part_o, sp};
+  p->tickets = tickets;
+  p->o = o;
+  p->lse = lse;
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_paged_decode(const void* q, const void* k_cache, const void* v_cache,
+                          const int* block_table, const int* seq_lens, void* o, float* lse,
+                          int num_seqs, int H, int Hkv, int d, int dv, int page_size,
+                          int num_pages, int max_blocks_per_seq, int num_splits, float scale,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  fa::DecodeParams p{};
+  bool nothing = false;
+  fa_status st = decode_setup("fa_paged_decode", q, k_cache, v_cache, block_table, seq_lens, o,
+                              lse, num_seqs, H, Hkv, d, dv, page_size, num_pages,
+                              max_blocks_per_seq, num_splits, scale, workspace, workspace_bytes,
+                              &p, &nothing);
+  if (st != FA_OK || nothing) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = fa::launch_decode_partials(p, s);
   if (e != cudaSuccess) return cuda_fail(e, "fa_paged_decode partials launch");
-  fa::CombineParams c{part_m, part_l, part_o, o, lse, num_seqs, H, num_splits, dv};
+  fa::CombineParams c{p.part_m, p.part_l, p.part_o, o, lse, num_seqs, H, num_splits, dv};
   e = fa::launch_split_combine(c, s);
   if (e != cudaSuccess) return cuda_fail(e, "fa_paged_decode combine launch");
+  return FA_OK;
+}
+
+fa_status fa_paged_decode_fused(const void* q, const void* k_cache, const void* v_cache,
+                                const int* block_table, const int* seq_lens, void* o, float* lse,
+                                int num_seqs, int H, int Hkv, int d, int dv, int page_size,
+                                int num_pages, int max_blocks_per_seq, int num_splits, float scale,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  fa::DecodeParams p{};
+  bool nothing = false;
+  fa_status st = decode_setup("fa_paged_decode_fused", q, k_cache, v_cache, block_table,
+                              seq_lens, o, lse, num_seqs, H, Hkv, d, dv, page_size, num_pages,
+                              max_blocks_per_seq, num_splits, scale, workspace, workspace_bytes,
+                              &p, &nothing);
+  if (st != FA_OK || nothing) return st;
+  cudaError_t e = fa::launch_decode(p, static_cast<cudaStream_t>(stream), true);
+  if (e != cudaSuccess) return cuda_fail(e, "fa_paged_decode_fused launch");
   return FA_OK;
 }
 

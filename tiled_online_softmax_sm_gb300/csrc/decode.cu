@@ -25,6 +25,11 @@
 // split_combine_kernel — one warp per (sequence, head): M = max m_x,
 //   w_x = exp(m_x - M), O = sum w_x o_x / sum w_x l_x, LSE = M + ln l.
 //
+// Fused form (decode_partials_kernel<true>, "S12 FlashAttention", 接下来: fuse
+//   the small-batch decode): the last split of each (sequence, kv head) to
+//   finish, found by an atomic ticket (no waiting on other warps), runs the
+//   same merge for the group's query heads in the same launch.
+//
 // decode_gather_kernel — a checking tool for the block-table walk: the
 //   decode's units, page ranges, lookups, tensor copies and swizzled page
 //   layout, with the gathered K and V rows copied out to dense buffers.
@@ -97,6 +102,92 @@ __device__ __forceinline__ void split_pages(int x, int X, int L, int& pb, int& p
   pe = (int)(((long long)(x + 1) * P + X - 1) / X);
 }
 
+// How the merge reads partials: through the read-only cache (the separate
+// merge kernel, whose partials were written by an earlier launch), or from L2
+// (the fused path, which reads partials other SMs wrote during the same
+// launch, after a fence).
+struct LoadReadOnly {
+  __device__ float operator()(const float* a) const { return __ldg(a); }
+  __device__ float4 v4(const float* a) const { return __ldg(reinterpret_cast<const float4*>(a)); }
+};
+struct LoadL2 {
+  __device__ float operator()(const float* a) const { return __ldcg(a); }
+  __device__ float4 v4(const float* a) const { return __ldcg(reinterpret_cast<const float4*>(a)); }
+};
+
+// Merge of the X split triples of one (sequence, head) t by one warp: M = max
+// m_x, w_x = exp(m_x - M) (0 for an empty split), O = sum w_x o_x / sum w_x
+// l_x, LSE = M + ln l.  The same arithmetic for either load policy, so the
+// separate and the fused merge give identical bits.
+template <typename Load>
+__device__ __forceinline__ void merge_splits(const float* __restrict__ part_m,
+                                             const float* __restrict__ part_l,
+                                             const float* __restrict__ part_o,
+                                             __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
+                                             size_t t, int X, int dv, int lane, Load load) {
+  const float* pm = part_m + t * X;
+  const float* pl = part_l + t * X;
+  // lane x holds split x and x + 32 (X <= 64): the weights are computed once
+  // and handed out by shuffles, so the o loads below are all independent
+  const float m0 = lane < X ? load(pm + lane) : -INFINITY;
+  const float m1 = lane + 32 < X ? load(pm + lane + 32) : -INFINITY;
+  float M = fmaxf(m0, m1);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  __nv_bfloat16* orow = o + t * dv;
+  if (M == -INFINITY) {
+    for (int c = lane * 4; c < dv; c += 128) {
+      *reinterpret_cast<uint2*>(orow + c) = make_uint2(0u, 0u);
+    }
+    if (lane == 0 && lse != nullptr) lse[t] = -INFINITY;
+    return;
+  }
+  const float w0 = m0 == -INFINITY ? 0.f : exp2f((m0 - M) * kLog2e);
+  const float w1 = m1 == -INFINITY ? 0.f : exp2f((m1 - M) * kLog2e);
+  float l = (lane < X ? w0 * load(pl + lane) : 0.f) + (lane + 32 < X ? w1 * load(pl + lane + 32) : 0.f);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  const float* po = part_o + t * X * dv;
+  // every lane runs every chunk (the shuffles need the whole warp); lanes
+  // past dv load and store nothing
+  for (int c0 = 0; c0 < dv; c0 += 128) {
+    const int c = c0 + lane * 4;
+    const bool active = c < dv;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int x0 = 0; x0 < X; x0 += 8) {
+      float4 v[8];
+      float w[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int x = x0 + u;
+        w[u] = __shfl_sync(0xffffffffu, x < 32 ? w0 : w1, x & 31);
+        v[u] = active && x < X ? load.v4(po + (size_t)x * dv + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        acc.x = fmaf(w[u], v[u].x, acc.x);
+        acc.y = fmaf(w[u], v[u].y, acc.y);
+        acc.z = fmaf(w[u], v[u].z, acc.z);
+        acc.w = fmaf(w[u], v[u].w, acc.w);
+      }
+    }
+    if (active) {
+      uint2 packed;
+      packed.x = ptx::pack_bf16x2(acc.x * inv, acc.y * inv);
+      packed.y = ptx::pack_bf16x2(acc.z * inv, acc.w * inv);
+      *reinterpret_cast<uint2*>(orow + c) = packed;
+    }
+  }
+  if (lane == 0 && lse != nullptr) lse[t] = l > 0.f ? M + logf(l) : -INFINITY;
+}
+
+// FUSED: after writing its triple, the warp takes a ticket of its (sequence,
+// kv head); the split that takes the last one merges the X triples of the G
+// query heads (merge_splits) and writes O and LSE, so no second launch is
+// needed.  Every unit takes its ticket, the timed-out ones included, and the
+// merging split sets the count back to 0 for the next call.
+template <bool FUSED>
 __global__ void __launch_bounds__(kWarps * 32)
 decode_partials_kernel(const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
@@ -104,7 +195,9 @@ decode_partials_kernel(const __grid_constant__ CUtensorMap tmK,
                        const int* __restrict__ seq_lens, int num_seqs, int H, int Hkv,
                        int num_pages, int max_blocks, int X, float scale_log2,
                        float* __restrict__ part_m, float* __restrict__ part_l,
-                       float* __restrict__ part_o, int* status, int skip_first_copy) {
+                       float* __restrict__ part_o, int* status, int skip_first_copy,
+                       int* __restrict__ tickets, __nv_bfloat16* __restrict__ o,
+                       float* __restrict__ lse) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -305,29 +398,46 @@ decode_partials_kernel(const __grid_constant__ CUtensorMap tmK,
       }
     }
     __syncwarp();
-    return;
-  }
-
+    if (!FUSED) return;
+  } else {
 #pragma unroll
-  for (int hr = 0; hr < 2; ++hr) {
-    l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 1);
-    l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 2);
-  }
-#pragma unroll
-  for (int hr = 0; hr < 2; ++hr) {
-    const int r = r0 + hr * 8;
-    if (r >= G) continue;
-    const size_t idx = ((size_t)s * H + g * G + r) * X + x;
-    if (!FA_IN_BOUNDS(idx, (size_t)num_seqs * H * X, status)) continue;
-    if ((lane & 3) == 0) {
-      part_m[idx] = m_run[hr] == -INFINITY ? -INFINITY : m_run[hr] * kLn2;
-      part_l[idx] = l_run[hr];
+    for (int hr = 0; hr < 2; ++hr) {
+      l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 1);
+      l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 2);
     }
-    float* orow = part_o + idx * kD;
 #pragma unroll
-    for (int j = 0; j < kD / 8; ++j)
-      *reinterpret_cast<float2*>(orow + j * 8 + c2) =
-          make_float2(oacc[j][hr * 2], oacc[j][hr * 2 + 1]);
+    for (int hr = 0; hr < 2; ++hr) {
+      const int r = r0 + hr * 8;
+      if (r >= G) continue;
+      const size_t idx = ((size_t)s * H + g * G + r) * X + x;
+      if (!FA_IN_BOUNDS(idx, (size_t)num_seqs * H * X, status)) continue;
+      if ((lane & 3) == 0) {
+        part_m[idx] = m_run[hr] == -INFINITY ? -INFINITY : m_run[hr] * kLn2;
+        part_l[idx] = l_run[hr];
+      }
+      float* orow = part_o + idx * kD;
+#pragma unroll
+      for (int j = 0; j < kD / 8; ++j)
+        *reinterpret_cast<float2*>(orow + j * 8 + c2) =
+            make_float2(oacc[j][hr * 2], oacc[j][hr * 2 + 1]);
+    }
+  }
+  if constexpr (FUSED) {
+    // The warp barrier orders every lane's triple stores before lane 0's
+    // ticket; the ticket is a release (this triple) and an acquire (the
+    // other splits' triples, for the unit that merges) at device scope; the
+    // second barrier passes the acquire on to the other lanes' loads.
+    __syncwarp();
+    int ticket = 0;
+    if (lane == 0) ticket = ptx::atom_add_acq_rel_gpu(tickets + (size_t)s * Hkv + g, 1);
+    ticket = __shfl_sync(0xffffffffu, ticket, 0);
+    __syncwarp();
+    if (ticket == X - 1) {
+      for (int r = 0; r < G; ++r)
+        merge_splits(part_m, part_l, part_o, o, lse, (size_t)s * H + g * G + r, X, kD, lane,
+                     LoadL2());
+      if (lane == 0) tickets[(size_t)s * Hkv + g] = 0;   // ready for the next call
+    }
   }
 }
 
@@ -338,62 +448,7 @@ split_combine_kernel(const float* __restrict__ part_m, const float* __restrict__
   const int t = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= pairs) return;
-  const float* pm = part_m + (size_t)t * X;
-  const float* pl = part_l + (size_t)t * X;
-  // lane x holds split x and x + 32 (X <= 64): the weights are computed once
-  // and handed out by shuffles, so the o loads below are all independent
-  const float m0 = lane < X ? __ldg(pm + lane) : -INFINITY;
-  const float m1 = lane + 32 < X ? __ldg(pm + lane + 32) : -INFINITY;
-  float M = fmaxf(m0, m1);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  __nv_bfloat16* orow = o + (size_t)t * dv;
-  if (M == -INFINITY) {
-    for (int c = lane * 4; c < dv; c += 128) {
-      *reinterpret_cast<uint2*>(orow + c) = make_uint2(0u, 0u);
-    }
-    if (lane == 0 && lse != nullptr) lse[t] = -INFINITY;
-    return;
-  }
-  const float w0 = m0 == -INFINITY ? 0.f : exp2f((m0 - M) * kLog2e);
-  const float w1 = m1 == -INFINITY ? 0.f : exp2f((m1 - M) * kLog2e);
-  float l = (lane < X ? w0 * __ldg(pl + lane) : 0.f) + (lane + 32 < X ? w1 * __ldg(pl + lane + 32) : 0.f);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-  const float inv = l > 0.f ? 1.f / l : 0.f;
-  const float* po = part_o + (size_t)t * X * dv;
-  // every lane runs every chunk (the shuffles need the whole warp); lanes
-  // past dv load and store nothing
-  for (int c0 = 0; c0 < dv; c0 += 128) {
-    const int c = c0 + lane * 4;
-    const bool active = c < dv;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int x0 = 0; x0 < X; x0 += 8) {
-      float4 v[8];
-      float w[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int x = x0 + u;
-        w[u] = __shfl_sync(0xffffffffu, x < 32 ? w0 : w1, x & 31);
-        v[u] = active && x < X ? __ldg(reinterpret_cast<const float4*>(po + (size_t)x * dv + c))
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        acc.x = fmaf(w[u], v[u].x, acc.x);
-        acc.y = fmaf(w[u], v[u].y, acc.y);
-        acc.z = fmaf(w[u], v[u].z, acc.z);
-        acc.w = fmaf(w[u], v[u].w, acc.w);
-      }
-    }
-    if (active) {
-      uint2 packed;
-      packed.x = ptx::pack_bf16x2(acc.x * inv, acc.y * inv);
-      packed.y = ptx::pack_bf16x2(acc.z * inv, acc.w * inv);
-      *reinterpret_cast<uint2*>(orow + c) = packed;
-    }
-  }
-  if (lane == 0 && lse != nullptr) lse[t] = l > 0.f ? M + logf(l) : -INFINITY;
+  merge_splits(part_m, part_l, part_o, o, lse, (size_t)t, X, dv, lane, LoadReadOnly());
 }
 
 // Block-table check: the decode's units (one warp per sequence, kv head and
@@ -476,7 +531,7 @@ int skip_first_copy_for_tests() {
 
 }  // namespace
 
-cudaError_t launch_decode_partials(const DecodeParams& p, cudaStream_t stream) {
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream, bool fused) {
   if (p.num_seqs == 0) return cudaSuccess;
   CUtensorMap tmK, tmV;
   const uint64_t rows = (uint64_t)p.num_pages * p.Hkv * kPage;
@@ -486,16 +541,22 @@ cudaError_t launch_decode_partials(const DecodeParams& p, cudaStream_t stream) {
   if (!make_tmap_bf16(&tmK, p.k_cache, 2, dims, strides, box) ||
       !make_tmap_bf16(&tmV, p.v_cache, 2, dims, strides, box))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(decode_partials_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  auto kernel = fused ? decode_partials_kernel<true> : decode_partials_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSmemBytes);
   if (e != cudaSuccess) return e;
   const int units = p.num_seqs * p.Hkv * p.num_splits;
   const int grid = (units + kWarps - 1) / kWarps;
-  decode_partials_kernel<<<grid, kWarps * 32, kSmemBytes, stream>>>(
+  kernel<<<grid, kWarps * 32, kSmemBytes, stream>>>(
       tmK, tmV, static_cast<const __nv_bfloat16*>(p.q), p.block_table, p.seq_lens, p.num_seqs,
       p.H, p.Hkv, p.num_pages, p.max_blocks, p.num_splits, p.scale * kLog2e, p.part_m, p.part_l,
-      p.part_o, p.status, skip_first_copy_for_tests());
+      p.part_o, p.status, skip_first_copy_for_tests(), p.tickets,
+      static_cast<__nv_bfloat16*>(p.o), p.lse);
   return cudaGetLastError();
+}
+
+cudaError_t launch_decode_partials(const DecodeParams& p, cudaStream_t stream) {
+  return launch_decode(p, stream, false);
 }
 
 cudaError_t launch_decode_gather(const GatherParams& p, cudaStream_t stream) {

@@ -136,7 +136,8 @@ extern "C" fa_status fa_paged_decode_noalloc(const void* q, const void* k_cache,
   void* scratch = nullptr;
   if ((st = scratch_address(&scratch)) != FA_OK) return st;
 
-  // same carving as the workspace of fa_paged_decode
+  // the partials carved as in fa_paged_decode's workspace (no ticket words:
+  // the merge runs as its own launch)
   const size_t tri = (size_t)num_seqs * H * num_splits;
   char* ws = static_cast<char*>(scratch);
   float* part_m = reinterpret_cast<float*>(ws);

@@ -102,6 +102,11 @@ struct DecodeParams {
   float* part_l;       // [S][H][X]
   float* part_o;       // [S][H][X][dv]
   int* status;
+  // fused form only: per (sequence, kv head) ticket counters, zero between
+  // calls, and the outputs the merging split writes
+  int* tickets = nullptr;
+  void* o = nullptr;   // bf16 [S][H][dv]
+  float* lse = nullptr;
 };
 
 struct CombineParams {
@@ -126,6 +131,8 @@ struct GatherParams {
 
 cudaError_t launch_fwd_f32(const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_fwd_bf16(const FwdParams& p, cudaStream_t stream, const char** why);
+// fused: partials and merge in one launch (p.tickets, p.o, p.lse set)
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream, bool fused);
 cudaError_t launch_decode_partials(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_split_combine(const CombineParams& p, cudaStream_t stream);
 cudaError_t launch_decode_gather(const GatherParams& p, cudaStream_t stream);

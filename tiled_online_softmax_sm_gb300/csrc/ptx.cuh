@@ -77,6 +77,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* st
   }
 }
 
+// Atomic add at device scope with acquire-release ordering; returns the old value.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* addr, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v)
+               : "memory");
+  return old;
+}
+
 // ------------------------------------------------- tensor copies (TMA)
 // 2-D / 3-D tiled copies global -> shared, completion counted on an mbarrier.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y,

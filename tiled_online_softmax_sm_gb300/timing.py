@@ -1,6 +1,7 @@
 """Device timing of every workload of the hot path, one table.
 
   python -m tiled_online_softmax_sm_gb300.timing [--iters 20] [--warmup 5]
+  python -m tiled_online_softmax_sm_gb300.timing --naive [--iters 20] [--warmup 5]
 
 Each workload runs on resident inputs from the seeded generators (the same
 as the tests and the bench).  A row reports the median of `iters` timed
@@ -14,6 +15,14 @@ decode, prefill and ragged inputs are larger than L2.  Rates use nominal work:
 4*n*m*d*H*B FLOPs (halved when causal; the ragged and paged rows sum their
 sequences), and for the decode the K and V bytes of every valid token.
 Nothing is checked here; parity lives in the tests.
+
+--naive times instead the materialised-score path against fa_forward at N =
+512, 2048 and 8192 (B=1, H=32, d=128, bf16, causal and not), the wall-clock
+side of "S12 FlashAttention", 练习 3 and 它还解锁了什么 (the 2-4x said to come
+from the HBM round trips of S): plain torch ops on the same inputs, S = (Q *
+scale) K^T in bf16, the causal mask written into S in place, a softmax over
+S (bf16 out, fp32 inside), then P V.  Each path gets its own best layout
+(head-major copies for the torch matmuls, made outside the timed region).
 """
 from __future__ import annotations
 
@@ -112,6 +121,17 @@ def rows(iters: int, warmup: int):
                                                    dc.dv, dc.page_size, dc.num_pages, dc.max_blocks,
                                                    X, dc.scale, ws, need), iters, warmup)
         out.append((f"paged decode 64 seqs H=32 Hkv=8 splits={X}", ms, dc.kv_bytes / (ms * 1e6), "GB/s"))
+    # the same decode in one launch (fa_paged_decode_fused), one zeroed workspace for all
+    wsf = torch.zeros(fb.fa_paged_decode_workspace_size(S, dc.H, dc.dv, 16), dtype=torch.uint8,
+                      device="cuda")
+    for X in (4, 8, 16):
+        od = torch.empty((S, dc.H, dc.dv), dtype=torch.bfloat16, device="cuda")
+        ld = torch.empty((S, dc.H), dtype=torch.float32, device="cuda")
+        ms = _median_ms(lambda: fb.fa_paged_decode_fused(qd, kc, vc, bt, sl, od, ld, S, dc.H, dc.Hkv,
+                                                         dc.d, dc.dv, dc.page_size, dc.num_pages,
+                                                         dc.max_blocks, X, dc.scale, wsf,
+                                                         wsf.numel()), iters, warmup)
+        out.append((f"paged decode fused 64 seqs H=32 Hkv=8 splits={X}", ms, dc.kv_bytes / (ms * 1e6), "GB/s"))
     # paged prefill: 512-token chunks of 16 sequences of the decode pool
     lens = I.uniform_lengths(63, 16, 512, 8192)
     ql = np.minimum(lens, 512)
@@ -147,11 +167,51 @@ def rows(iters: int, warmup: int):
     return out
 
 
+def naive_vs_tiled(iters: int, warmup: int, sizes=(512, 2048, 8192), H: int = 32, D: int = 128):
+    """Rows (N, causal, naive ms, tiled ms, S bytes) for the materialised-score
+    path and fa_forward on the same bf16 inputs."""
+    out = []
+    scale = I.fp32_scale(D)
+    for N in sizes:
+        g = torch.Generator(device="cuda").manual_seed(N)
+        q = torch.randn(1, N, H, D, device="cuda", generator=g).bfloat16()
+        k = torch.randn(1, N, H, D, device="cuda", generator=g).bfloat16()
+        v = torch.randn(1, N, H, D, device="cuda", generator=g).bfloat16()
+        o = torch.empty_like(q)
+        lse = torch.empty(1, H, N, device="cuda")
+        qh, kh, vh = (x[0].transpose(0, 1).contiguous() for x in (q, k, v))   # [H, N, D]
+        masked = torch.ones(N, N, dtype=torch.bool, device="cuda").tril().logical_not_()
+        for causal in (True, False):
+            def naive():
+                s = torch.matmul(qh * scale, kh.transpose(-1, -2))           # [H, N, N] bf16
+                if causal:
+                    s.masked_fill_(masked, float("-inf"))
+                p = torch.softmax(s, dim=-1)
+                return torch.matmul(p, vh)
+
+            naive_ms = _median_ms(naive, iters, warmup)
+            tiled_ms = _median_ms(lambda: fb.fa_forward(q, k, v, o, lse, 1, H, H, N, N, D, D, scale,
+                                                         int(causal)), iters, warmup)
+            out.append((N, causal, naive_ms, tiled_ms, H * N * N * 2))
+        del q, k, v, o, lse, qh, kh, vh, masked
+        torch.cuda.empty_cache()
+    return out
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--naive", action="store_true",
+                    help="time the materialised-score path against fa_forward instead")
     a = ap.parse_args(argv)
+    if a.naive:
+        print("| N | causal | materialised S (torch) | fa_forward | ratio | bf16 S size |\n"
+              "|---|---|---|---|---|---|")
+        for N, causal, naive_ms, tiled_ms, s_bytes in naive_vs_tiled(a.iters, a.warmup):
+            print(f"| {N} | {causal} | {naive_ms:.3f} ms | {tiled_ms:.3f} ms | "
+                  f"{naive_ms / tiled_ms:.1f}x | {s_bytes / 2**20:.0f} MiB |", flush=True)
+        return 0
     print(f"| workload | median time | rate |\n|---|---|---|")
     for name, ms, rate, unit in rows(a.iters, a.warmup):
         t = f"{ms * 1000:.1f} us" if ms < 1 else f"{ms:.3f} ms"
