@@ -56,6 +56,20 @@ def test_small_shapes(shape):
     _check_full(I.dense_case(31, B, H, n, m, d, Hkv=Hkv, causal=causal, name=f"bf16_{shape}"))
 
 
+@pytest.mark.parametrize("shape", [
+    # B, H, Hkv, n, m, d: pair units B*H*ceil(n/256) past the 152 SMs, so the
+    # last wave runs as split units (one query tile, keys halved between the
+    # two warpgroups, merged in the CTA)
+    (1, 160, 160, 256, 300, 128),    # 160 units: 8 in the last wave
+    (1, 158, 79, 200, 1000, 64),     # a ragged second query tile, grouped heads
+    (2, 80, 40, 512, 129, 128),      # 320 units: 16 in the last wave, 2 K/V tiles each
+    (1, 170, 170, 256, 1024, 64),    # 18 in the last wave
+])
+def test_last_wave_split_units(shape):
+    B, H, Hkv, n, m, d = shape
+    _check_full(I.dense_case(35, B, H, n, m, d, Hkv=Hkv, causal=False, name=f"split {shape}"))
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_hot_x10(causal):
     _check_full(I.dense_case(32, 1, 2, 640, 640, 128, causal=causal, hot=10.0, name="hot"))

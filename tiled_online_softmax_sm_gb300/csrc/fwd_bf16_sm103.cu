@@ -39,6 +39,12 @@
 // loaded or multiplied ("手搓 Attention" §6).  Causal is aligned bottom-right:
 // query i of n sees keys j <= i + (m - n) (top-left when n == m).
 //
+// Dense non-causal launches whose last wave of pair units would leave at
+// least half the CTAs idle run those units as split units instead: one query
+// tile whose K/V tiles are halved between the two softmax warpgroups, the two
+// (m, l, O) states merged at the end inside the CTA with the same rescale
+// ("S12 FlashAttention", 练习 1), so the last wave takes about half as long.
+//
 // Every mbarrier wait is bounded; on a timeout the CTA records it in the
 // device status word, stops issuing work, lets copies in flight land and
 // frees its tensor memory.
@@ -112,17 +118,27 @@ struct Shared {
   uint64_t kv_empty[8];
   uint64_t drain;
   uint64_t fix;         // paged: a V tile that reaches past the end, before zeroing
+  uint64_t merge_full;  // split unit: warpgroup 1's row states are in mstat
+  uint64_t merge_empty; // split unit: warpgroup 0 has read them
+  float mstat[kBlockM][3];  // split unit: (m, l, l_p) of each row of warpgroup 1
   uint32_t tmem_base;
   int abort;
 };
 
 // One work unit: a pair of 128-row query tiles of one (sequence, head).
+// A split unit (dense, the last partial wave only) is one query tile whose
+// K/V tiles are halved between the two softmax warpgroups: both Q slots hold
+// the same rows, tile 1 starts at K/V tile kv_first[1], and warpgroup 0 merges
+// the two (m, l, O) states at the end, reading O_1 from tensor memory.
 struct Unit {
   int b, h, hk;
   int q_len, kv_len, q_row0, k_row0, q_start0;
+  int q_start[2];  // first query row (in the sequence) of each tile
+  int kv_first[2]; // first K/V tile of each tile
   int n_kv[2];     // K/V tiles each query tile needs (0: tile inactive)
   bool rows;       // the unit holds at least one valid query row
   bool bad;        // varlen offsets outside the buffers
+  bool split;      // the two tiles are one query tile over two key ranges
 };
 
 // Row max of a 128-key S row: 8 independent chains of three-input max (one
@@ -266,13 +282,36 @@ __device__ __forceinline__ Unit make_unit(int b, int h, int t, int H, int Hkv, i
   }
   U.q_start0 = t * 2 * kBlockM;
   U.rows = !U.bad && U.q_start0 < U.q_len;
+  U.split = false;
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const int qs = U.q_start0 + i * kBlockM;
+    U.q_start[i] = qs;
+    U.kv_first[i] = 0;
     int keys = U.kv_len;   // causal: the tile's last row sees keys < qs + 128 + (m - n)
     if (causal) keys = min(U.kv_len, qs + kBlockM + (U.kv_len - U.q_len));
     U.n_kv[i] = (!U.rows || qs >= U.q_len || keys <= 0) ? 0 : (keys + kBlockN - 1) / kBlockN;
   }
+  return U;
+}
+
+// Query tile `tile` of the pair unit R as a split unit: its K/V tiles halved
+// between the two warpgroups.  A query tile with one K/V tile stays a plain
+// one-tile unit (tile 1 inactive).
+__device__ __forceinline__ Unit split_unit(Unit R, int tile) {
+  Unit U = R;
+  // selects, not R.x[tile]: a runtime index would put the unit in local memory
+  const int n = tile == 0 ? R.n_kv[0] : R.n_kv[1];
+  const int qs = tile == 0 ? R.q_start[0] : R.q_start[1];
+  const int half = (n + 1) / 2;
+  U.q_start[0] = U.q_start[1] = qs;
+  U.q_start0 = qs;
+  U.rows = R.rows && n > 0;
+  U.n_kv[0] = half;
+  U.n_kv[1] = n - half;
+  U.kv_first[0] = 0;
+  U.kv_first[1] = half;
+  U.split = U.n_kv[1] > 0;
   return U;
 }
 
@@ -290,7 +329,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 int total_k, int num_pairs, float scale_log2, int causal, int lse_stride_h,
                 int lse_stride_b, const int* __restrict__ block_table,
                 const int* __restrict__ seq_lens, int max_blocks, int num_pages, float out_scale,
-                int sched_sorted, int* status) {
+                int sched_sorted, int num_split, int* status) {
   using C = Cfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ Shared sh;
@@ -334,14 +373,20 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     if (mine) atomicAdd(&sh.n_order, mine);
     __syncthreads();
   }
-  const int num_units = VAR && sched_sorted ? H * sh.n_order : BH * num_pairs;
+  // Dense: the last num_split pair units (the partial last wave) are run as
+  // 2 * num_split split units, one per query tile, so that wave finishes in
+  // about half a unit's time.
+  const int num_units = VAR && sched_sorted ? H * sh.n_order : BH * num_pairs + (VAR ? 0 : num_split);
   auto unit_at = [&](int u) {
     if (VAR && sched_sorted) {
       const int c = sh.order[u / H];
       return unit_bt(c / num_pairs, u % H, c % num_pairs);
     }
-    const int bh = u % BH;
-    return unit_bt(bh / H, bh % H, num_pairs - 1 - u / BH);
+    const int base = BH * num_pairs - (VAR ? 0 : num_split);
+    const int r = u < base ? u : base + (u - base) / 2;
+    const int bh = r % BH;
+    const Unit R = unit_bt(bh / H, bh % H, num_pairs - 1 - r / BH);
+    return u < base ? R : split_unit(R, (u - base) & 1);
   };
 #define FA_UNIT(u) unit_at(u)
   // k-th unit of this CTA: waves of gridDim.x units in snake order (even waves
@@ -365,9 +410,12 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const uint32_t bar_kve = ptx::smem_u32(&sh.kv_empty[0]);
   const uint32_t bar_drain = ptx::smem_u32(&sh.drain);
   const uint32_t bar_fix = ptx::smem_u32(&sh.fix);
+  const uint32_t bar_mf = ptx::smem_u32(&sh.merge_full);
+  const uint32_t bar_me = ptx::smem_u32(&sh.merge_empty);
   volatile int* abort_flag = &sh.abort;
 
   if (threadIdx.x == 0) {
+    #pragma unroll
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(bar_q + 8 * i, 1);
       ptx::mbar_init(bar_qe + 8 * i, 1);
@@ -382,6 +430,8 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     }
     ptx::mbar_init(bar_drain, 1);
     ptx::mbar_init(bar_fix, 1);
+    ptx::mbar_init(bar_mf, kBlockM);
+    ptx::mbar_init(bar_me, kBlockM);
     sh.abort = 0;
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
@@ -421,6 +471,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const Unit U = FA_UNIT(u);
         if (U.bad && lane == 0) atomicExch(status, kDevInvalidArg);  // skip it, touch nothing
         if (!U.rows) continue;
+        #pragma unroll
         for (int i = 0; i < 2 && ok; ++i) {
           if (U.n_kv[i] == 0) continue;
           // the previous unit's last S_i MMA must be done with Q_i
@@ -431,17 +482,16 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
 #pragma unroll
             for (int c = 0; c < C::kChunks; ++c)
               ptx::tma_load_3d_hint(dst + c * 16384, &tmQ, C::kChunkElems * c, U.h,
-                                    U.q_row0 + U.q_start0 + i * kBlockM, bar_q + 8 * i, pol_q);
+                                    U.q_row0 + U.q_start[i], bar_q + 8 * i, pol_q);
           }
           ++nq[i];
         }
-        const int n_kv_max = max(U.n_kv[0], U.n_kv[1]);
-        for (int j = 0; j < n_kv_max && ok; ++j) {
-          for (int which = 0; which < 2 && ok; ++which) {  // K then V
+        // one K (which 0) or V (which 1) tile load into the next ring slot;
+        // false if a wait failed
+        auto issue_kv = [&](int which, int j) __attribute__((always_inline)) -> bool {
             const int slot = li % C::kStages;
-            if (!(ok = ptx::mbar_wait(bar_kve + 8 * slot, ((li / C::kStages) & 1) ^ 1, status,
-                                      abort_flag)))
-              break;
+            if (!ptx::mbar_wait(bar_kve + 8 * slot, ((li / C::kStages) & 1) ^ 1, status, abort_flag))
+              return false;
             __syncwarp();
             uint8_t* tile = sKV + slot * C::kTileBytes;
             const uint32_t dst = ptx::smem_u32(tile);
@@ -494,7 +544,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             }
             if (fix) {
               fix_pending = true;
-              if (!(ok = ptx::mbar_wait(bar_fix, nfix & 1, status, abort_flag))) break;
+              if (!ptx::mbar_wait(bar_fix, nfix & 1, status, abort_flag)) return false;
               fix_pending = false;
               ++nfix;
               const int zero_rows = kBlockN - rows_valid;
@@ -510,7 +560,24 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
               if (lane == 0) ptx::mbar_arrive(bar_kvf + 8 * slot);
             }
             ++li;
-          }
+            return true;
+        };
+        const int n_kv_max = max(U.n_kv[0], U.n_kv[1]);
+        if (!U.split) {
+          for (int j = 0; j < n_kv_max && ok; ++j)
+            for (int which = 0; which < 2 && ok; ++which) ok = issue_kv(which, j);  // K then V
+        } else {
+          // the MMA warp's order for a split unit: K_0(0), K_1(0), then per
+          // step V_0(j), K_0(j+1), V_1(j), K_1(j+1) (tile i's K/V tiles
+          // start at kv_first[i])
+          #pragma unroll
+          for (int i = 0; i < 2 && ok; ++i) ok = issue_kv(0, U.kv_first[i]);
+          for (int j = 0; j < U.n_kv[0] && ok; ++j)
+            #pragma unroll
+            for (int i = 0; i < 2 && ok; ++i) {
+              if (j < U.n_kv[i]) ok = issue_kv(1, U.kv_first[i] + j);
+              if (ok && j + 1 < U.n_kv[i]) ok = issue_kv(0, U.kv_first[i] + j + 1);
+            }
         }
       }
       if (!ok && lane == 0) {
@@ -518,6 +585,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // shared memory is released
         for (int l = max(0, li - C::kStages); l < li; ++l)
           ptx::mbar_wait(bar_kvf + 8 * (l % C::kStages), (l / C::kStages) & 1, nullptr);
+        #pragma unroll
         for (int i = 0; i < 2; ++i)
           if (nq[i] > 0) ptx::mbar_wait(bar_q + 8 * i, (nq[i] - 1) & 1, nullptr);
         if (fix_pending) ptx::mbar_wait(bar_fix, nfix & 1, nullptr);
@@ -576,17 +644,65 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         if (!U.rows) continue;
         const int n_kv_max = max(U.n_kv[0], U.n_kv[1]);
         if (n_kv_max == 0) continue;
+        #pragma unroll
         for (int i = 0; i < 2 && ok; ++i) {
           if (U.n_kv[i] == 0) continue;
           ok = ptx::mbar_wait(bar_q + 8 * i, nq[i] & 1, status, abort_flag);
           ++nq[i];
         }
         if (!ok) break;
+        if (U.split) {
+          // Split unit: each tile has its own K/V tiles, consumed in the
+          // producer's order (K_0(0), K_1(0), then per step V_0(j), K_0(j+1),
+          // V_1(j), K_1(j+1)); each slot is released right behind its MMAs.
+          // wait for the next ring slot in load order; its index is lc - 1 after
+          auto next_slot = [&]() -> bool {
+            const bool w = ptx::mbar_wait(bar_kvf + 8 * (lc % C::kStages), (lc / C::kStages) & 1,
+                                          status, abort_flag);
+            ++lc;
+            if (w) ptx::tc_fence_after();
+            return w;
+          };
+          #pragma unroll
+          for (int i = 0; i < 2 && ok; ++i) {
+            if (!(ok = next_slot())) break;
+            const int slot = (lc - 1) % C::kStages;
+            issue_s(i, slot);
+            ptx::tc_commit(bar_s + 8 * i);
+            if (U.n_kv[i] == 1) ptx::tc_commit(bar_qe + 8 * i);
+            ptx::tc_commit(bar_kve + 8 * slot);
+          }
+          for (int j = 0; j < U.n_kv[0] && ok; ++j) {
+            #pragma unroll
+            for (int i = 0; i < 2 && ok; ++i) {
+              if (j >= U.n_kv[i]) continue;
+              if (!(ok = next_slot())) break;
+              const int slot = (lc - 1) % C::kStages;
+              if (j == 0 && !(ok = ptx::mbar_wait(bar_oe + 8 * i, (no[i] & 1) ^ 1, status, abort_flag))) break;
+              if (!(ok = issue_pv(i, slot, j))) break;
+              if (j == U.n_kv[i] - 1) ptx::tc_commit(bar_o + 8 * i);
+              ptx::tc_commit(bar_kve + 8 * slot);
+              if (j + 1 < U.n_kv[i]) {
+                if (!(ok = next_slot())) break;
+                const int sk = (lc - 1) % C::kStages;
+                issue_s(i, sk);
+                ptx::tc_commit(bar_s + 8 * i);
+                if (j + 2 == U.n_kv[i]) ptx::tc_commit(bar_qe + 8 * i);
+                ptx::tc_commit(bar_kve + 8 * sk);
+              }
+            }
+          }
+          #pragma unroll
+          for (int i = 0; i < 2; ++i)
+            if (U.n_kv[i] > 0) ++no[i];
+          continue;
+        }
         // prologue: S_i(0)
         {
           const int slot = lc % C::kStages;
           if (!(ok = ptx::mbar_wait(bar_kvf + 8 * slot, (lc / C::kStages) & 1, status, abort_flag))) break;
           ptx::tc_fence_after();
+          #pragma unroll
           for (int i = 0; i < 2; ++i) {
             if (U.n_kv[i] == 0) continue;
             issue_s(i, slot);
@@ -633,6 +749,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           }
         }
         lc += 2 * n_kv_max;
+        #pragma unroll
         for (int i = 0; i < 2; ++i)
           if (U.n_kv[i] > 0) ++no[i];
       }
@@ -650,16 +767,19 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const uint32_t s_col = lane_base + i * kBlockN;
     const uint32_t o_col = lane_base + 256 + i * D;
     int ns = 0;    // S tiles consumed
-    int nod = 0;   // units finished
+    int nod[2] = {0, 0};   // units whose tile 0 / tile 1 had K/V tiles (o_done phases)
+    int nsplit = 0;        // split units seen (merge barrier phases)
     bool ok = true;
     for (int k = 0; k * (int)gridDim.x < num_units && ok; ++k) {
       const int u = unit_of(k);
       if (u >= num_units) continue;
       const Unit U = FA_UNIT(u);
       if (!U.rows) continue;
-      const int q_start = U.q_start0 + i * kBlockM;
+      // (selects, not U.x[i]: a runtime index would put the unit in local memory)
+      const int q_start = i == 0 ? U.q_start[0] : U.q_start[1];
+      const int kv_first = i == 0 ? U.kv_first[0] : U.kv_first[1];
       const int qi = q_start + r;               // query index in the sequence
-      const int nkv = U.n_kv[i];
+      const int nkv = i == 0 ? U.n_kv[0] : U.n_kv[1];
       float m_ref = -INFINITY;   // running reference (log2 units)
       bool max_first = false;    // this warp forms P max-first for the rest of the unit
       float l_run = 0.f;         // sum of the unrounded p: the LSE's l
@@ -672,7 +792,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         ptx::tc_fence_after();
         // mask keys past the end and, causal, keys j > qi + (m - n): only tiles
         // that reach past the end or past the tile's first row's diagonal
-        const int k0 = j * kBlockN;
+        const int k0 = (kv_first + j) * kBlockN;
         const int diag = q_start + (U.kv_len - U.q_len);   // last key row q_start sees
         const bool masked = k0 + kBlockN > U.kv_len || (causal && k0 + kBlockN - 1 > diag);
         int vis = U.kv_len - k0;
@@ -765,11 +885,80 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       // ---- epilogue: O = acc / l (bf16), LSE = (ref + log2 l) ln 2
       const bool row_valid = qi < U.q_len;
       const size_t orow = (size_t)(U.q_row0 + qi) * H + U.h;
+      const int ph_o0 = nod[0] & 1, ph_o1 = nod[1] & 1, ph_m = nsplit & 1;
+      if (U.n_kv[0] > 0) ++nod[0];
+      if (U.n_kv[1] > 0) ++nod[1];
+      if (U.split) {
+        ++nsplit;
+        if (i == 1) {
+          // hand this row's state to warpgroup 0, which merges the two halves
+          ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar_me, ph_m ^ 1, status, abort_flag));
+          if (!ok) break;
+          sh.mstat[r][0] = m_ref;
+          sh.mstat[r][1] = l_run;
+          sh.mstat[r][2] = l_p;
+          ptx::mbar_arrive(bar_mf);
+          continue;
+        }
+        // M = max of the two references, a_i = 2^(m_i - M) (0 for a state
+        // that saw no key); O = (a_0 acc_0 + a_1 acc_1) / (a_0 l_0 + a_1 l_1)
+        // with the rounded sums, LSE from the exact ones
+        ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar_o, ph_o0, status, abort_flag) &&
+                                         ptx::mbar_wait(bar_o + 8, ph_o1, status, abort_flag) &&
+                                         ptx::mbar_wait(bar_mf, ph_m, status, abort_flag));
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const float m1 = sh.mstat[r][0], l1 = sh.mstat[r][1], lp1 = sh.mstat[r][2];
+        ptx::mbar_arrive(bar_me);
+        const float M = fmaxf(m_ref, m1);
+        const float a0 = m_ref == -INFINITY ? 0.f : ptx::ex2(m_ref - M);
+        const float a1 = m1 == -INFINITY ? 0.f : ptx::ex2(m1 - M);
+        const float l_all = a0 * l_run + a1 * l1;
+        const float lo_all = FP8 ? l_all : a0 * l_p + a1 * lp1;
+        const float inv = lo_all > 0.f ? out_scale / lo_all : 0.f;
+        const float c0 = a0 * inv, c1 = a1 * inv;
+        const uint32_t o_col1 = lane_base + 256 + D;
+        const bool store = row_valid && FA_IN_BOUNDS(orow, (size_t)total_q * H, status);
+        uint4* dst = reinterpret_cast<uint4*>(o + orow * D);
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t x0[32], x1[32];
+          ptx::tmem_ld32(o_col + c * 32, x0);
+          ptx::tmem_ld32(o_col1 + c * 32, x1);
+          ptx::tmem_wait_ld();
+          if (store) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              float f[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                f[e] = __uint_as_float(x0[8 * w + e]) * c0 + __uint_as_float(x1[8 * w + e]) * c1;
+              uint4 v;
+              v.x = ptx::pack_bf16x2(f[0], f[1]);
+              v.y = ptx::pack_bf16x2(f[2], f[3]);
+              v.z = ptx::pack_bf16x2(f[4], f[5]);
+              v.w = ptx::pack_bf16x2(f[6], f[7]);
+              dst[c * 4 + w] = v;
+            }
+          }
+        }
+        // both O accumulators may now be overwritten by the next unit
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_oe);
+        ptx::mbar_arrive(bar_oe + 8);
+        if (store) {
+          const size_t li = (size_t)U.b * lse_stride_b + (size_t)U.h * lse_stride_h +
+                            (U.q_row0 - (cu_q ? 0 : U.b * n)) + qi;
+          if (lse != nullptr && FA_IN_BOUNDS(li, (size_t)total_q * H, status))
+            lse[li] = l_all > 0.f ? (M + __log2f(l_all)) * kLn2 : -INFINITY;
+        }
+        continue;
+      }
       uint32_t ov[D / 32][32];
       if (nkv > 0) {
-        ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar_o + 8 * i, nod & 1, status, abort_flag));
+        ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar_o + 8 * i, i == 0 ? ph_o0 : ph_o1, status,
+                                                    abort_flag));
         if (!ok) break;
-        ++nod;
         ptx::tc_fence_after();
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) ptx::tmem_ld32(o_col + c * 32, ov[c]);
@@ -887,6 +1076,15 @@ cudaError_t launch(const FwdParams& p, cudaStream_t stream, const char** why) {
   // depend on lengths the host does not know (idle units exit at once).
   const bool sorted = varlen && (long long)p.B * num_pairs <= kMaxSortedCombos;
   const int grid = varlen && !sorted ? (int)units : (int)(units < sms ? units : sms);
+  // Dense and non-causal (units of equal size): when the last wave of pair
+  // units would leave at least half the CTAs idle, those units run as twice
+  // as many split units of about half the length.  Causal units already
+  // shrink towards the end of the heaviest-first order.
+  int num_split = 0;
+  if (!varlen && !PAGED && !p.causal && (p.m + kBlockN - 1) / kBlockN >= 2) {
+    const long long tail = units % grid;
+    if (tail > 0 && 2 * tail <= grid) num_split = (int)tail;
+  }
   // LSE layout: dense [B][H][n] ; varlen and paged [H][Tq]
   const int lse_stride_h = varlen ? p.total_q : p.n;
   const int lse_stride_b = varlen ? 0 : p.H * p.n;
@@ -904,7 +1102,7 @@ cudaError_t launch(const FwdParams& p, cudaStream_t stream, const char** why) {
         tq, tk, tv, static_cast<__nv_bfloat16*>(p.o), p.lse, p.cu_q, p.cu_k, p.B, p.H, p.Hkv, p.n,
         p.m, varlen ? p.total_q : p.B * p.n, varlen ? p.total_k : p.B * p.m, num_pairs, scale_log2,
         p.causal, lse_stride_h, lse_stride_b, p.block_table, p.seq_lens, p.max_blocks, p.num_pages,
-        out_scale, sorted ? 1 : 0, p.status);
+        out_scale, sorted ? 1 : 0, num_split, p.status);
     err = cudaGetLastError();
     if (err != cudaSuccess) *why = "fwd_bf16 launch";
     return err;
