@@ -284,18 +284,27 @@ def config_table(peaks):
     from tiled_online_softmax_sm_gb300 import inputs as I
     from tiled_online_softmax_sm_gb300 import timing
 
+    # e4m3: the library's own dense e4m3 GEMM rate measured here, else the
+    # nominal ratio (4.5 vs 2.25 PFLOP/s) times the measured bf16 peak
+    fp8_peak = timing.fp8_gemm_peak()
+    fp8_note = ("measured e4m3 GEMM (cuBLASLt) %.1f TFLOP/s" % fp8_peak if fp8_peak
+                else "2 x the measured bf16 peak (no e4m3 GEMM measured)")
+
     def frac(name, rate, unit):
         if name.startswith("fp32"):
             return None   # a few microseconds: bound by latency, not by a pipe
         if unit == "GB/s":
             return round(rate / peaks["hbm_gbs"], 4)
-        # e4m3 runs at twice the bf16 tensor rate (nominal 4.5 vs 2.25 PFLOP/s)
-        peak = peaks["bf16_tflops"] * (2.0 if name.startswith("e4m3") else 1.0)
-        return round(rate / peak, 4)
+        if name.startswith("e4m3"):
+            return round(rate / (fp8_peak or 2.0 * peaks["bf16_tflops"]), 4)
+        return round(rate / peaks["bf16_tflops"], 4)
 
     table = {name: {"gpu": {"ms": round(ms, 4), "rate": round(rate, 2), "unit": unit,
                             "frac": frac(name, rate, unit)}}
              for name, ms, rate, unit in timing.rows(20, 5)}
+    for name in table:
+        if name.startswith("e4m3"):
+            table[name]["gpu"]["peak"] = fp8_note
     c1 = I.c1_fp32()
     c1_flops = 4.0 * 256 * 256 * 64
     all_threads = oracle.num_threads()

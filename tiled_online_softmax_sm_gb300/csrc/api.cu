@@ -371,7 +371,7 @@ fa_status fa_paged_decode(const void* q, const void* k_cache, const void* v_cach
   cudaError_t e = fa::launch_decode_partials(p, s);
   if (e != cudaSuccess) return cuda_fail(e, "fa_paged_decode partials launch");
   fa::CombineParams c{p.part_m, p.part_l, p.part_o, o, lse, num_seqs, H, num_splits, dv};
-  e = fa::launch_split_combine(c, s);
+  e = fa::launch_split_combine(c, s, true);
   if (e != cudaSuccess) return cuda_fail(e, "fa_paged_decode combine launch");
   return FA_OK;
 }

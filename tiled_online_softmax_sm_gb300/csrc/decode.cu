@@ -220,6 +220,9 @@ decode_partials_kernel(const __grid_constant__ CUtensorMap tmK,
     }
     __syncthreads();
   }
+  // the merge launched behind this kernel may start once every CTA of this
+  // one is running (it waits for this kernel's completion before reading)
+  asm volatile("griddepcontrol.launch_dependents;");
   if (unit >= num_seqs * Hkv * X) return;
 
   const int x = unit % X;
@@ -445,6 +448,10 @@ __global__ void __launch_bounds__(128)
 split_combine_kernel(const float* __restrict__ part_m, const float* __restrict__ part_l,
                      const float* __restrict__ part_o, __nv_bfloat16* __restrict__ o,
                      float* __restrict__ lse, int pairs, int X, int dv) {
+  // Launched right behind the partials kernel as a programmatic dependent, the
+  // merge's blocks may start during that kernel's tail: wait here until it
+  // has completed and its partials are visible (at once without a predecessor).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int t = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= pairs) return;
@@ -578,13 +585,29 @@ cudaError_t launch_decode_gather(const GatherParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_split_combine(const CombineParams& p, cudaStream_t stream) {
+cudaError_t launch_split_combine(const CombineParams& p, cudaStream_t stream, bool behind_partials) {
   const int pairs = p.num_seqs * p.H;
   if (pairs == 0) return cudaSuccess;
-  split_combine_kernel<<<(pairs + 3) / 4, 128, 0, stream>>>(
-      p.part_m, p.part_l, p.part_o, static_cast<__nv_bfloat16*>(p.o), p.lse, pairs, p.num_splits,
-      p.dv);
-  return cudaGetLastError();
+  if (!behind_partials) {
+    split_combine_kernel<<<(pairs + 3) / 4, 128, 0, stream>>>(
+        p.part_m, p.part_l, p.part_o, static_cast<__nv_bfloat16*>(p.o), p.lse, pairs,
+        p.num_splits, p.dv);
+    return cudaGetLastError();
+  }
+  // programmatic dependent launch: the merge's launch overlaps the partials
+  // kernel's tail instead of starting after it has drained
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((pairs + 3) / 4));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, split_combine_kernel, p.part_m, p.part_l, p.part_o,
+                            static_cast<__nv_bfloat16*>(p.o), p.lse, pairs, p.num_splits, p.dv);
 }
 
 }  // namespace fa

@@ -134,7 +134,10 @@ cudaError_t launch_fwd_bf16(const FwdParams& p, cudaStream_t stream, const char*
 // fused: partials and merge in one launch (p.tickets, p.o, p.lse set)
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream, bool fused);
 cudaError_t launch_decode_partials(const DecodeParams& p, cudaStream_t stream);
-cudaError_t launch_split_combine(const CombineParams& p, cudaStream_t stream);
+// behind_partials: launched right after launch_decode_partials on the same
+// stream, as a programmatic dependent of it
+cudaError_t launch_split_combine(const CombineParams& p, cudaStream_t stream,
+                                 bool behind_partials = false);
 cudaError_t launch_decode_gather(const GatherParams& p, cudaStream_t stream);
 
 }  // namespace fa

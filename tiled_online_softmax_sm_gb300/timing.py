@@ -167,6 +167,25 @@ def rows(iters: int, warmup: int):
     return out
 
 
+def fp8_gemm_peak(n: int = 8192, reps: int = 10):
+    """Dense e4m3 GEMM rate of the library GEMM (cuBLASLt through
+    torch._scaled_mm, bf16 out), n x n x n, best of reps: the denominator for
+    the e4m3 forward's fraction.  None if this torch build has no e4m3 GEMM
+    for the device."""
+    try:
+        a = torch.randn(n, n, device="cuda").to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device="cuda").to(torch.float8_e4m3fn).t()   # column-major operand
+        one = torch.ones((), device="cuda")
+        mm = lambda: torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        for _ in range(3):
+            mm()
+        best = min(_median_ms(mm, 1, 0) for _ in range(reps))
+        del a, b
+        return 2.0 * n ** 3 / (best * 1e9)
+    except (RuntimeError, AttributeError, TypeError) as e:  # no e4m3 GEMM in this build
+        return None
+
+
 def naive_vs_tiled(iters: int, warmup: int, sizes=(512, 2048, 8192), H: int = 32, D: int = 128):
     """Rows (N, causal, naive ms, tiled ms, S bytes) for the materialised-score
     path and fa_forward on the same bf16 inputs."""
@@ -204,7 +223,14 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--naive", action="store_true",
                     help="time the materialised-score path against fa_forward instead")
+    ap.add_argument("--fp8-peak", action="store_true",
+                    help="print the dense e4m3 GEMM rate of the library GEMM and exit")
     a = ap.parse_args(argv)
+    if a.fp8_peak:
+        r = fp8_gemm_peak()
+        print(f"e4m3 GEMM 8192^3 (cuBLASLt via torch._scaled_mm): "
+              + ("unavailable" if r is None else f"{r:.1f} TFLOP/s"))
+        return 0
     if a.naive:
         print("| N | causal | materialised S (torch) | fa_forward | ratio | bf16 S size |\n"
               "|---|---|---|---|---|---|")
