@@ -678,13 +678,15 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
               if (j >= U.n_kv[i]) continue;
               if (!(ok = next_slot())) break;
               const int slot = (lc - 1) % C::kStages;
+              // K_i(j+1) before P_i(j), as in the pair loop below
+              const bool nxt = j + 1 < U.n_kv[i];
+              if (nxt && !(ok = next_slot())) break;
+              const int sk = (lc - 1) % C::kStages;
               if (j == 0 && !(ok = ptx::mbar_wait(bar_oe + 8 * i, (no[i] & 1) ^ 1, status, abort_flag))) break;
               if (!(ok = issue_pv(i, slot, j))) break;
               if (j == U.n_kv[i] - 1) ptx::tc_commit(bar_o + 8 * i);
               ptx::tc_commit(bar_kve + 8 * slot);
-              if (j + 1 < U.n_kv[i]) {
-                if (!(ok = next_slot())) break;
-                const int sk = (lc - 1) % C::kStages;
+              if (nxt) {
                 issue_s(i, sk);
                 ptx::tc_commit(bar_s + 8 * i);
                 if (j + 2 == U.n_kv[i]) ptx::tc_commit(bar_qe + 8 * i);
@@ -716,6 +718,13 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           const int lk = lc + 2 * j + 2, sk = lk % C::kStages;
           const bool has_next = j + 1 < n_kv_max;
           if (!(ok = ptx::mbar_wait(bar_kvf + 8 * sv, (lv / C::kStages) & 1, status, abort_flag))) break;
+          // K(j+1) is waited for here, before P_0(j): it has landed long
+          // before P_0(j) is ready, and a wait between P_0 V(j) and
+          // S_0(j+1) would leave the tensor pipe idle behind P_0 V(j)
+          if (has_next &&
+              !(ok = ptx::mbar_wait(bar_kvf + 8 * sk, (lk / C::kStages) & 1, status, abort_flag)))
+            break;
+          ptx::tc_fence_after();
           // before the first P V of a unit, the previous unit's epilogue must
           // have read O_i out of tensor memory
           if (j < U.n_kv[0]) {
@@ -727,10 +736,6 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           // iteration) here, behind a burst of queued MMAs rather than in the
           // gap after S_1(j); K(0) was released in the prologue
           if (j > 0) ptx::tc_commit(bar_kve + 8 * ((lc + 2 * j) % C::kStages));
-          if (has_next) {
-            if (!(ok = ptx::mbar_wait(bar_kvf + 8 * sk, (lk / C::kStages) & 1, status, abort_flag))) break;
-            ptx::tc_fence_after();
-          }
           if (j + 1 < U.n_kv[0]) {
             issue_s(0, sk);
             ptx::tc_commit(bar_s);
