@@ -17,7 +17,8 @@
 //                 one query row = one tensor-memory lane, so row max and row
 //                 sum need no shuffles.
 //   Tensor memory: S_0 | S_1 (128 fp32 columns each), O_0 | O_1 (d columns
-//   each).  P_i (bf16) overwrites the first 64 columns of S_i; the next
+//   each; at d = 64 in bf16, 80 columns at 128-column spacing, the last 16
+//   holding l_p).  P_i (bf16) overwrites the first 64 columns of S_i; the next
 //   S_i MMA is issued after the P_i V MMA, and tcgen05 MMAs of one thread
 //   execute in issue order.
 //
@@ -30,7 +31,9 @@
 // Two row sums are kept: l of the exact p, for LSE = (ref + log2 l) ln 2, and
 // l_p of the bf16-rounded p the P V MMA multiplies, for O = acc / l_p, so that
 // O is a weighted mean of V rows whose weights sum to one whatever the
-// rounding (a row one key dominates gets that key's V row back).  The row max
+// rounding (a row one key dominates gets that key's V row back).  At d = 64
+// the tensor core forms l_p itself, as extra columns of the P V product with
+// a block of ones; at d = 128 the softmax threads add up the packed P.  The row max
 // itself is taken only when needed: p is first formed
 // against the current ref, and a tile row sum of at most 256 proves no raise
 // is due (see the softmax loop).  While a row has seen only
@@ -91,13 +94,22 @@ struct Cfg {
   static constexpr int kChunks = kRowBytes / 128;           // chunks per row
   static constexpr int kKStep = 32 / kElem;                 // reduction length of one MMA (32 bytes)
   static constexpr int kTileBytes = 128 * kRowBytes;        // Q, K or V tile
-  static constexpr int kStages = kTileBytes == 32768 ? 4 : 8;   // K/V ring slots
+  // bf16 at d = 64: the P V MMA is 16 columns wider than V, and its B operand
+  // reads those columns from a block of ones that sits right behind the V
+  // tile in every ring slot, so O's accumulator carries l_p (the sum of the
+  // bf16 P it multiplied) in columns D .. D+15, accumulated and rescaled by
+  // the tensor core with O.  (At d = 128 the tensor memory has no room left.)
+  static constexpr bool kOnes = D == 64 && !FP8;
+  static constexpr int kSlotBytes = kOnes ? 2 * kTileBytes : kTileBytes;  // ring slot stride
+  static constexpr int kStages = kOnes ? 5 : kTileBytes == 32768 ? 4 : 8;  // K/V ring slots
+  static constexpr int kON = kOnes ? D + 16 : D;           // O accumulator columns
+  static constexpr int kOStride = kOnes ? 128 : D;         // tensor-memory columns between O_0 and O_1
   static constexpr int kQBytes = 2 * kTileBytes;
-  static constexpr int kSmem = kQBytes + kStages * kTileBytes + 1024;  // + alignment slack
+  static constexpr int kSmem = kQBytes + kStages * kSlotBytes + 1024;  // + alignment slack
   static constexpr uint32_t kIdescS = FP8 ? ptx::idesc_e4m3_f32(128, kBlockN, false, false)
                                           : ptx::idesc_bf16_f32(128, kBlockN, false, false);
   static constexpr uint32_t kIdescO = FP8 ? ptx::idesc_e4m3_f32(128, D, false, true)
-                                          : ptx::idesc_bf16_f32(128, D, false, true);
+                                          : ptx::idesc_bf16_f32(128, kON, false, true);
 };
 
 // Varlen and paged launches with at most this many (sequence, query pair)
@@ -398,7 +410,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   };
 
   uint8_t* sQ = smem;                        // [2][kChunks][128 rows][128 B]
-  uint8_t* sKV = smem + C::kQBytes;          // [kStages][kChunks][128 rows][128 B]
+  uint8_t* sKV = smem + C::kQBytes;          // [kStages][kChunks (+1 of ones)][128 rows][128 B]
 
   const uint32_t bar_q = ptx::smem_u32(&sh.q_full[0]);
   const uint32_t bar_qe = ptx::smem_u32(&sh.q_empty[0]);
@@ -435,6 +447,16 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     sh.abort = 0;
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
+  }
+  if constexpr (C::kOnes) {
+    // the block of ones behind every ring slot's tile: bf16 1.0 in every
+    // element, so the swizzle does not matter; K and V loads never reach it
+    constexpr int kWords = C::kTileBytes / 16;
+    for (int idx = threadIdx.x; idx < C::kStages * kWords; idx += kThreads)
+      *reinterpret_cast<uint4*>(sKV + (idx / kWords) * C::kSlotBytes + C::kTileBytes +
+                                (idx % kWords) * 16) =
+          make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    ptx::fence_proxy_async_smem();   // visible to the tensor core after the barrier below
   }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(&sh.tmem_base), 512);
@@ -493,7 +515,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             if (!ptx::mbar_wait(bar_kve + 8 * slot, ((li / C::kStages) & 1) ^ 1, status, abort_flag))
               return false;
             __syncwarp();
-            uint8_t* tile = sKV + slot * C::kTileBytes;
+            uint8_t* tile = sKV + slot * C::kSlotBytes;
             const uint32_t dst = ptx::smem_u32(tile);
             const CUtensorMap* map = which == 0 ? &tmK : &tmV;
             const int rows_valid = min(kBlockN, U.kv_len - j * kBlockN);
@@ -607,7 +629,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       const uint64_t kdesc0 = ptx::smem_desc_sw128(ptx::smem_u32(sKV), 16, 1024);
       const uint64_t vdesc0 = ptx::smem_desc_sw128(ptx::smem_u32(sKV), 16384, 1024);
       auto issue_s = [&](int i, int slot) {
-        const uint64_t kd = kdesc0 + (uint64_t)(slot * (C::kTileBytes >> 4));
+        const uint64_t kd = kdesc0 + (uint64_t)(slot * (C::kSlotBytes >> 4));
 #pragma unroll
         for (int k = 0; k < C::kRowBytes / 32; ++k) {
           const uint32_t off = ((k >> 2) * 16384 + (k & 3) * 32) >> 4;
@@ -620,7 +642,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       // O_i += P_i V(j), issued once the softmax warps have stored all of
       // P_i; false if the wait failed
       auto issue_pv = [&](int i, int slot, int j) -> bool {
-        const uint64_t vd = vdesc0 + (uint64_t)(slot * (C::kTileBytes >> 4));
+        const uint64_t vd = vdesc0 + (uint64_t)(slot * (C::kSlotBytes >> 4));
         if (!ptx::mbar_wait(bar_p + 8 * i, np[i] & 1, status, abort_flag)) return false;
         ptx::tc_fence_after();
 #pragma unroll
@@ -628,10 +650,10 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           // a step covers kKStep keys: 8 packed P columns, kKStep V rows of 128 B
           const uint64_t bd = vd + (uint64_t)(k * C::kKStep * 8);
           if constexpr (FP8)
-            ptx::mma_ts_f8(tbase + 256 + i * D, tbase + i * kBlockN + k * 8, bd, C::kIdescO,
+            ptx::mma_ts_f8(tbase + 256 + i * C::kOStride, tbase + i * kBlockN + k * 8, bd, C::kIdescO,
                            (j > 0 || k > 0) ? 1u : 0u);
           else
-            ptx::mma_ts(tbase + 256 + i * D, tbase + i * kBlockN + k * 8, bd, C::kIdescO,
+            ptx::mma_ts(tbase + 256 + i * C::kOStride, tbase + i * kBlockN + k * 8, bd, C::kIdescO,
                         (j > 0 || k > 0) ? 1u : 0u);
         }
         ++np[i];
@@ -770,7 +792,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     const int r = quarter * 32 + lane;        // row in the tile
     const uint32_t lane_base = tbase + ((uint32_t)(quarter * 32) << 16);
     const uint32_t s_col = lane_base + i * kBlockN;
-    const uint32_t o_col = lane_base + 256 + i * D;
+    const uint32_t o_col = lane_base + 256 + i * C::kOStride;
     int ns = 0;    // S tiles consumed
     int nod[2] = {0, 0};   // units whose tile 0 / tile 1 had K/V tiles (o_done phases)
     int nsplit = 0;        // split units seen (merge barrier phases)
@@ -861,7 +883,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           // tile: no P V of this tile may run before it
           if (__any_sync(0xffffffffu, raise && j > 0 && alpha != 1.f)) {
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < (C::kON + 31) / 32; ++c) {   // with l_p's columns
               uint32_t ov[32];
               ptx::tmem_ld32(o_col + c * 32, ov);
               ptx::tmem_wait_ld();
@@ -883,7 +905,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         // that key's V row back to within fp32 rounding, where the exact sum
         // would leave the rounding of that key's p (up to 2^-8 relative) in O.
         // Done after the hand-off, while the MMAs run.
-        if constexpr (!FP8) l_p += sum_packed_bf16(pp);
+        if constexpr (!FP8 && !C::kOnes) l_p += sum_packed_bf16(pp);
       }
       if (!ok) break;
 
@@ -913,7 +935,17 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                                          ptx::mbar_wait(bar_mf, ph_m, status, abort_flag));
         if (!ok) break;
         ptx::tc_fence_after();
-        const float m1 = sh.mstat[r][0], l1 = sh.mstat[r][1], lp1 = sh.mstat[r][2];
+        const uint32_t o_col1 = lane_base + 256 + C::kOStride;   // O_1: the other key range
+        const float m1 = sh.mstat[r][0], l1 = sh.mstat[r][1];
+        float lp1 = sh.mstat[r][2];
+        if constexpr (C::kOnes) {   // both rounded sums sit in column D of their O
+          uint32_t t0[32], t1[32];
+          ptx::tmem_ld32(o_col + D, t0);
+          ptx::tmem_ld32(o_col1 + D, t1);
+          ptx::tmem_wait_ld();
+          l_p = __uint_as_float(t0[0]);
+          lp1 = __uint_as_float(t1[0]);
+        }
         ptx::mbar_arrive(bar_me);
         const float M = fmaxf(m_ref, m1);
         const float a0 = m_ref == -INFINITY ? 0.f : ptx::ex2(m_ref - M);
@@ -922,7 +954,6 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const float lo_all = FP8 ? l_all : a0 * l_p + a1 * lp1;
         const float inv = lo_all > 0.f ? out_scale / lo_all : 0.f;
         const float c0 = a0 * inv, c1 = a1 * inv;
-        const uint32_t o_col1 = lane_base + 256 + D;
         const bool store = row_valid && FA_IN_BOUNDS(orow, (size_t)total_q * H, status);
         uint4* dst = reinterpret_cast<uint4*>(o + orow * D);
 #pragma unroll 1
@@ -967,6 +998,12 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         ptx::tc_fence_after();
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) ptx::tmem_ld32(o_col + c * 32, ov[c]);
+        if constexpr (C::kOnes) {   // the rounded sum from O's column D
+          uint32_t t[32];
+          ptx::tmem_ld32(o_col + D, t);
+          ptx::tmem_wait_ld();
+          l_p = __uint_as_float(t[0]);
+        }
         ptx::tmem_wait_ld();
         // O_i may now be overwritten by the next unit's first P V
         ptx::tc_fence_before();
