@@ -70,6 +70,32 @@ def test_last_wave_split_units(shape):
     _check_full(I.dense_case(35, B, H, n, m, d, Hkv=Hkv, causal=False, name=f"split {shape}"))
 
 
+@pytest.mark.parametrize("shape", [
+    # B, H, Hkv, n, m, d, causal: pair units, and (last row) split units
+    (1, 2, 1, 300, 300, 128, True),
+    (2, 3, 3, 517, 517, 64, False),
+    (1, 160, 160, 256, 300, 128, False),
+])
+def test_output_on_a_16_byte_boundary_gives_the_same_bits(shape):
+    """O that starts 16 bytes past a 32-byte boundary is written with 16-byte
+    stores instead of 32-byte ones: the bits must not change."""
+    B, H, Hkv, n, m, d, causal = shape
+    c = I.dense_case(36, B, H, n, m, d, Hkv=Hkv, causal=causal, name=f"o16 {shape}")
+    q, k, v = dev(c.q), dev(c.k), dev(c.v)
+    o_a, lse_a = fb.forward(q, k, v, c.scale, causal)
+    numel = B * n * H * d
+    buf = torch.empty(numel + 64, dtype=torch.bfloat16, device="cuda")
+    off = (16 - buf.data_ptr() % 32) % 32 // 2   # elements to 16 bytes past a 32-byte boundary
+    o_b = buf[off:off + numel].view(B, n, H, d)
+    assert o_b.data_ptr() % 32 == 16
+    lse_b = torch.empty_like(lse_a)
+    fb.fa_forward(q, k, v, o_b, lse_b, B, H, Hkv, n, m, d, d, c.scale, causal)
+    torch.cuda.synchronize()
+    assert fb.fa_get_device_status() == 0
+    assert torch.equal(o_a.view(torch.int16), o_b.view(torch.int16))
+    assert torch.equal(lse_a, lse_b)
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_hot_x10(causal):
     _check_full(I.dense_case(32, 1, 2, 640, 640, 128, causal=causal, hot=10.0, name="hot"))

@@ -797,6 +797,19 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     int nod[2] = {0, 0};   // units whose tile 0 / tile 1 had K/V tiles (o_done phases)
     int nsplit = 0;        // split units seen (merge barrier phases)
     bool ok = true;
+    // 64 bytes of a row of O: rows are 2D bytes, so when O starts on a
+    // 32-byte boundary every 32 bytes go out in one store (a whole sector),
+    // half the store instructions and L2 writes of the 16-byte form
+    const bool o32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
+    auto store_o64 = [&](uint4* dst, const uint4 (&v)[4]) __attribute__((always_inline)) {
+      if (o32) {
+        ptx::st_global_v8(dst, v[0], v[1]);
+        ptx::st_global_v8(dst + 2, v[2], v[3]);
+      } else {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) dst[w] = v[w];
+      }
+    };
     for (int k = 0; k * (int)gridDim.x < num_units && ok; ++k) {
       const int u = unit_of(k);
       if (u >= num_units) continue;
@@ -963,19 +976,19 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           ptx::tmem_ld32(o_col1 + c * 32, x1);
           ptx::tmem_wait_ld();
           if (store) {
+            uint4 v[4];
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
               float f[8];
 #pragma unroll
               for (int e = 0; e < 8; ++e)
                 f[e] = __uint_as_float(x0[8 * w + e]) * c0 + __uint_as_float(x1[8 * w + e]) * c1;
-              uint4 v;
-              v.x = ptx::pack_bf16x2(f[0], f[1]);
-              v.y = ptx::pack_bf16x2(f[2], f[3]);
-              v.z = ptx::pack_bf16x2(f[4], f[5]);
-              v.w = ptx::pack_bf16x2(f[6], f[7]);
-              dst[c * 4 + w] = v;
+              v[w].x = ptx::pack_bf16x2(f[0], f[1]);
+              v[w].y = ptx::pack_bf16x2(f[2], f[3]);
+              v[w].z = ptx::pack_bf16x2(f[4], f[5]);
+              v[w].w = ptx::pack_bf16x2(f[6], f[7]);
             }
+            store_o64(dst + c * 4, v);
           }
         }
         // both O accumulators may now be overwritten by the next unit
@@ -1022,16 +1035,17 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const float inv = l_o > 0.f ? out_scale / l_o : 0.f;
         uint4* dst = reinterpret_cast<uint4*>(o + orow * D);
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c)
+        for (int c = 0; c < D / 32; ++c) {
+          uint4 v[4];
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
-            uint4 v;
-            v.x = ptx::pack_bf16x2(__uint_as_float(ov[c][8 * w + 0]) * inv, __uint_as_float(ov[c][8 * w + 1]) * inv);
-            v.y = ptx::pack_bf16x2(__uint_as_float(ov[c][8 * w + 2]) * inv, __uint_as_float(ov[c][8 * w + 3]) * inv);
-            v.z = ptx::pack_bf16x2(__uint_as_float(ov[c][8 * w + 4]) * inv, __uint_as_float(ov[c][8 * w + 5]) * inv);
-            v.w = ptx::pack_bf16x2(__uint_as_float(ov[c][8 * w + 6]) * inv, __uint_as_float(ov[c][8 * w + 7]) * inv);
-            dst[c * 4 + w] = v;
+            v[w].x = ptx::pack_bf16x2(__uint_as_float(ov[c][8 * w + 0]) * inv, __uint_as_float(ov[c][8 * w + 1]) * inv);
+            v[w].y = ptx::pack_bf16x2(__uint_as_float(ov[c][8 * w + 2]) * inv, __uint_as_float(ov[c][8 * w + 3]) * inv);
+            v[w].z = ptx::pack_bf16x2(__uint_as_float(ov[c][8 * w + 4]) * inv, __uint_as_float(ov[c][8 * w + 5]) * inv);
+            v[w].w = ptx::pack_bf16x2(__uint_as_float(ov[c][8 * w + 6]) * inv, __uint_as_float(ov[c][8 * w + 7]) * inv);
           }
+          store_o64(dst + c * 4, v);
+        }
         const size_t li = (size_t)U.b * lse_stride_b + (size_t)U.h * lse_stride_h +
                           (U.q_row0 - (cu_q ? 0 : U.b * n)) + qi;
         if (lse != nullptr && FA_IN_BOUNDS(li, (size_t)total_q * H, status))

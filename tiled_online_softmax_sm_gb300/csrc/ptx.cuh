@@ -77,6 +77,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* st
   }
 }
 
+// 32 bytes to global memory in one store; p must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* p, uint4 lo, uint4 hi) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(lo.x),
+               "r"(lo.y), "r"(lo.z), "r"(lo.w), "r"(hi.x), "r"(hi.y), "r"(hi.z), "r"(hi.w)
+               : "memory");
+}
+
 // Atomic add at device scope with acquire-release ordering; returns the old value.
 __device__ __forceinline__ int atom_add_acq_rel_gpu(int* addr, int v) {
   int old;
