@@ -838,7 +838,24 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         int vis = U.kv_len - k0;
         if (causal) vis = min(vis, qi + (U.kv_len - U.q_len) - k0 + 1);
         uint32_t sr[4][32];
-        auto load_s = [&]() {
+        // S into registers.  Where the row max is wanted (a unit's first tile,
+        // a max-first warp, the reload after a miss) and no key is masked, the
+        // loads reduce it themselves (tcgen05.ld.red ... .max): the hardware
+        // max of each thread's 32 columns, so the 43 three-input max of
+        // row_max are not spent.  Masked tiles take row_max after masking,
+        // since the loads would see the masked scores too.
+        float mred = -INFINITY;
+        bool have_mred = false;
+        auto load_s = [&](bool want_max) {
+          if (!masked && want_max) {
+            float mc[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) ptx::tmem_ld32_max(s_col + c * 32, sr[c], mc[c]);
+            ptx::tmem_wait_ld();
+            mred = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]));
+            have_mred = true;
+            return;
+          }
 #pragma unroll
           for (int c = 0; c < 4; ++c) ptx::tmem_ld32(s_col + c * 32, sr[c]);
           ptx::tmem_wait_ld();
@@ -850,7 +867,7 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                 if (c * 32 + e >= vis) sr[c][e] = __float_as_uint(-INFINITY);
           }
         };
-        load_s();
+        load_s(j == 0 || max_first);
         // From the second tile on, P is first formed against the current
         // reference without the row max.  Every p is at most the tile's row
         // sum, so a sum of at most 2^threshold shows that no score passed the
@@ -876,12 +893,12 @@ fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           full = __any_sync(0xffffffffu, !(lsum <= kRaiseSum) || m_ref == -INFINITY);
           max_first = full;
           if constexpr (!FP8) {
-            if (full) load_s();
+            if (full) load_s(true);
             else ptx::tmem_st64(s_col, pp);
           }
         }
         if (full) {
-          const float m_tile = row_max(sr) * scale_log2;   // scale > 0: max commutes with it
+          const float m_tile = (have_mred ? mred : row_max(sr)) * scale_log2;   // scale > 0: max commutes with it
           const bool raise =
               m_tile > m_ref + kRescaleThreshold || (m_ref == -INFINITY && m_tile > -INFINITY);
           float alpha = 1.f;
