@@ -26,18 +26,27 @@ namespace {
 // 256-row problem is only 256 rows): measured on GB300 at n = m = 256, d = 64,
 // 4 lanes 92 us, 8 lanes 66 us, 16 lanes 60 us per launch.
 constexpr int kThreadsPerRow = 16;
-constexpr int kGroupThreads = 128;                          // one key group
-constexpr int kRowsPerCta = kGroupThreads / kThreadsPerRow;  // query rows per CTA
-// The CTA's key tiles are dealt to kGroups groups of 128 threads (tile t to
-// group t % kGroups), each with its own rows' state and tile buffer, and the
-// groups' (max, sum, acc) are merged at the end the way split partials are
-// ("S12 FlashAttention", 它还解锁了什么): a row's key tiles run side by side.
-constexpr int kGroups = 4;
-constexpr int kThreads = kGroupThreads * kGroups;
+// Key groups of a CTA: the CTA's key tiles are dealt to its groups (tile t to
+// group t % kGroups), each with its own copy of the rows' state and its own
+// tile buffer, and the groups' (max, sum, acc) are merged at the end the way
+// split partials are ("S12 FlashAttention", 它还解锁了什么): a row's key tiles
+// run side by side.  The kernel is bound by latency, so more and smaller CTAs
+// with more groups finish sooner: at n = m = 256, d = 64, groups of 128
+// threads x 4 took 21.3 us, groups of 64 x 8 took 11.8 us (GB300).  Eight
+// groups of d = dv = 128 tiles would need 256 KB of shared memory, so that
+// instance keeps 128 x 4.
+template <int D, int DV>
+struct Shape {
+  static constexpr bool kSmall = D + DV <= 192;
+  static constexpr int kGroupThreads = kSmall ? 64 : 128;           // one key group
+  static constexpr int kGroups = kSmall ? 8 : 4;
+  static constexpr int kRowsPerCta = kGroupThreads / kThreadsPerRow;  // query rows per CTA
+  static constexpr int kThreads = kGroupThreads * kGroups;
+};
 
-// bar.sync on a named barrier of the kGroupThreads threads of one group
-__device__ __forceinline__ void group_sync(int group) {
-  asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(kGroupThreads) : "memory");
+// bar.sync on the named barrier of one group (count: the group's threads)
+__device__ __forceinline__ void group_sync(int group, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(count) : "memory");
 }
 constexpr int kTileN = 32;                      // keys per K/V tile
 constexpr float kLog2e = 1.4426950408889634f;
@@ -77,13 +86,14 @@ __device__ __forceinline__ float pair_diff_scaled(float a_hi, float a_lo, float 
 }
 
 template <int D, int DV>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(Shape<D, DV>::kThreads)
 fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
                const float* __restrict__ v, float* __restrict__ o, float* __restrict__ lse,
                int B, int H, int Hkv, int n, int m, float scale, int causal, int* status) {
+  using S = Shape<D, DV>;
   extern __shared__ float4 smem4[];
-  const int group = threadIdx.x / kGroupThreads;
-  const int tid = threadIdx.x % kGroupThreads;   // thread within its group
+  const int group = threadIdx.x / S::kGroupThreads;
+  const int tid = threadIdx.x % S::kGroupThreads;   // thread within its group
   float4* sK = smem4 + group * kTileN * ((D + DV) / 4);   // [kTileN][D/4] of this group
   float4* sV = sK + kTileN * (D / 4);                     // [kTileN][DV/4]
 
@@ -93,7 +103,7 @@ fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
   const int h = blockIdx.y;
   const int b = blockIdx.z;
   const int hk = h / (H / Hkv);
-  const int q0 = blockIdx.x * kRowsPerCta;
+  const int q0 = blockIdx.x * S::kRowsPerCta;
   const int i = q0 + row;                       // query index of this row
   const bool row_valid = i < n;
 
@@ -117,26 +127,26 @@ fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
 
   int kv_end = m;
   const int off = m - n;  // causal, bottom-right: query i sees keys j <= i + off
-  if (causal) kv_end = min(m, q0 + kRowsPerCta + off);
+  if (causal) kv_end = min(m, q0 + S::kRowsPerCta + off);
   const size_t k_row_stride = (size_t)Hkv * D;
   const size_t v_row_stride = (size_t)Hkv * DV;
   const float* kbase = k + ((size_t)b * m * Hkv + hk) * D;
   const float* vbase = v + ((size_t)b * m * Hkv + hk) * DV;
 
-  for (int j0 = group * kTileN; j0 < kv_end; j0 += kGroups * kTileN) {
+  for (int j0 = group * kTileN; j0 < kv_end; j0 += S::kGroups * kTileN) {
     const int cols = min(kTileN, m - j0);
-    group_sync(group);  // previous tile fully consumed
-    for (int idx = tid; idx < kTileN * (D / 4); idx += kGroupThreads) {
+    group_sync(group, S::kGroupThreads);  // previous tile fully consumed
+    for (int idx = tid; idx < kTileN * (D / 4); idx += S::kGroupThreads) {
       int r = idx / (D / 4), c = idx % (D / 4);
       sK[idx] = r < cols ? reinterpret_cast<const float4*>(kbase + (size_t)(j0 + r) * k_row_stride)[c]
                          : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    for (int idx = tid; idx < kTileN * (DV / 4); idx += kGroupThreads) {
+    for (int idx = tid; idx < kTileN * (DV / 4); idx += S::kGroupThreads) {
       int r = idx / (DV / 4), c = idx % (DV / 4);
       sV[idx] = r < cols ? reinterpret_cast<const float4*>(vbase + (size_t)(j0 + r) * v_row_stride)[c]
                          : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    group_sync(group);
+    group_sync(group, S::kGroupThreads);
 
     int vis = cols;                 // visible keys of this row in the tile: [0, vis)
     if (causal) vis = min(vis, i + off - j0 + 1);
@@ -207,9 +217,9 @@ fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
   // ---- merge the groups: each publishes (max pair, sum, acc) of its rows;
   // group 0 rescales them to the common max and adds them up
   __syncthreads();   // every group is done with its tile buffer
-  float* st = reinterpret_cast<float*>(smem4);   // [kGroups][kRowsPerCta][4 + DV]
+  float* st = reinterpret_cast<float*>(smem4);   // [S::kGroups][S::kRowsPerCta][4 + DV]
   constexpr int kRowFloats = 4 + DV;   // max pair, sum, a pad word: acc stays 16-byte aligned
-  float* mine = st + (group * kRowsPerCta + row) * kRowFloats;
+  float* mine = st + (group * S::kRowsPerCta + row) * kRowFloats;
   if (part == 0) {
     mine[0] = m_hi;
     mine[1] = m_lo;
@@ -221,8 +231,8 @@ fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
   __syncthreads();
   if (group != 0) return;
   float g_hi = -INFINITY, g_lo = 0.f;   // max over the groups
-  for (int g = 0; g < kGroups; ++g) {
-    const float* o_g = st + (g * kRowsPerCta + row) * kRowFloats;
+  for (int g = 0; g < S::kGroups; ++g) {
+    const float* o_g = st + (g * S::kRowsPerCta + row) * kRowFloats;
     if (o_g[0] > g_hi) {
       g_hi = o_g[0];
       g_lo = o_g[1];
@@ -232,8 +242,8 @@ fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
 #pragma unroll
   for (int c = 0; c < VC; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (g_hi != -INFINITY) {
-    for (int g = 0; g < kGroups; ++g) {
-      const float* o_g = st + (g * kRowsPerCta + row) * kRowFloats;
+    for (int g = 0; g < S::kGroups; ++g) {
+      const float* o_g = st + (g * S::kRowsPerCta + row) * kRowFloats;
       if (o_g[0] == -INFINITY) continue;   // this group saw no key of the row
       const float w = exp2f(pair_diff_scaled(o_g[0], o_g[1], g_hi, g_lo, scale_log2));
       l_run = fmaf(w, o_g[2], l_run);
@@ -267,14 +277,15 @@ fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
 
 template <int D, int DV>
 cudaError_t launch(const FwdParams& p, cudaStream_t stream) {
-  const size_t tiles = sizeof(float) * kTileN * (D + DV) * kGroups;
-  const size_t merge = sizeof(float) * kGroups * kRowsPerCta * (4 + DV);
+  using S = Shape<D, DV>;
+  const size_t tiles = sizeof(float) * kTileN * (D + DV) * S::kGroups;
+  const size_t merge = sizeof(float) * S::kGroups * S::kRowsPerCta * (4 + DV);
   const size_t smem = tiles > merge ? tiles : merge;
   cudaError_t e = cudaFuncSetAttribute(fwd_f32_kernel<D, DV>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((p.n + kRowsPerCta - 1) / kRowsPerCta, p.H, p.B);
-  fwd_f32_kernel<D, DV><<<grid, kThreads, smem, stream>>>(
+  dim3 grid((p.n + S::kRowsPerCta - 1) / S::kRowsPerCta, p.H, p.B);
+  fwd_f32_kernel<D, DV><<<grid, S::kThreads, smem, stream>>>(
       static_cast<const float*>(p.q), static_cast<const float*>(p.k),
       static_cast<const float*>(p.v), static_cast<float*>(p.o), p.lse, p.B, p.H, p.Hkv, p.n,
       p.m, p.scale, p.causal, p.status);
